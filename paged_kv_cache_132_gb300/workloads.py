@@ -1,0 +1,279 @@
+"""Seeded synthetic decode workloads, shared by the GPU path and the oracle.
+
+This module only draws inputs: context lengths, block tables and slot numbers
+(through the host block manager), and normally distributed payloads for the
+KV pools, queries and new tokens.  It holds none of the attention arithmetic.
+
+The five workloads stand in for the pages' evaluation workloads (which use
+the ShareGPT/Alpaca/WMT16 datasets and OPT/LLaMA weights, none of which is
+used here); their shapes follow the models the pages evaluate:
+
+  tiny               4 seqs, ctx {5,17,33,64}, 4 heads (MHA), d 64, fp32, B 16,
+                     32-block pool in a seeded random order.
+  opt13b             64 seqs, 40 heads (MHA), d 128, fp16, B 16, ctx ~ U[128,2048],
+                     pool 1.1x the blocks needed, random block order.
+  llama8b            256 seqs, 32 query / 8 KV heads, d 128, bf16, B 16,
+                     ctx = clip(round(LogNormal(ln 1024, 1.0)), 16, 8192),
+                     pool = exactly the blocks needed, shuffled.
+  parallel_sampling  32 prompts x 8 samples, llama8b head shape, bf16, B 16;
+                     1000-token prompt shared through reference counts, tails
+                     ~ U[0,512] per sample; copy-on-write of the partial last
+                     prompt block (7 copies per prompt) before the tails are
+                     written; pool 1.1x the blocks used, shuffled.
+  long_context       16 seqs x 32768 ctx, llama8b head shape, bf16, shuffled,
+                     512-token partitions; block size 8, 16 or 32 (same tokens).
+
+Every workload describes one decode step: (1) the copy-on-write pairs (only
+parallel_sampling has any), (2) the new tokens' K/V and their slots, (3) the
+queries, with context lengths that include the token written in (2).  Slots
+not holding a cached token are filled with NaN, so a kernel that lets a stale
+slot reach its sums fails every comparison.
+
+Payloads are drawn on ``device`` with a generator seeded from the workload's
+seed; the integer structure (lengths, tables, slots) is always drawn on the
+CPU, so it is identical for every device.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+from typing import Dict, List, Optional
+
+import torch
+
+from .block_manager import BlockManager, blocks_needed
+
+SEED_BASE = 132000
+
+WORKLOADS = ("tiny", "opt13b", "llama8b", "parallel_sampling", "long_context")
+_INDEX = {name: i for i, name in enumerate(WORKLOADS)}
+
+
+@dataclass
+class Workload:
+    name: str
+    num_seqs: int
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    dtype: torch.dtype
+    num_blocks: int
+    scale: float
+    partition_size: int              # 0: the library picks
+    context_lens: torch.Tensor       # int32 [S], includes this step's token
+    block_tables: torch.Tensor       # int32 [S][max_blocks], -1 past each table
+    query: torch.Tensor              # [S][H][d]
+    k_cache: torch.Tensor            # [NB][Hkv][B][d], before the step
+    v_cache: torch.Tensor
+    new_key: torch.Tensor            # [T][Hkv][d]
+    new_value: torch.Tensor
+    slot_mapping: torch.Tensor       # int64 [T]
+    copy_pairs: torch.Tensor         # int64 [n][2] (src, dst)
+    seed: int = 0
+    notes: Dict[str, object] = field(default_factory=dict)
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max().item()) if self.num_seqs else 0
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.slot_mapping.numel())
+
+    def to(self, device) -> "Workload":
+        moved = {}
+        for f in ("context_lens", "block_tables", "query", "k_cache", "v_cache", "new_key",
+                  "new_value", "slot_mapping", "copy_pairs"):
+            moved[f] = getattr(self, f).to(device)
+        return replace(self, **moved)
+
+
+# ---------------------------------------------------------------------------
+# integer structure
+# ---------------------------------------------------------------------------
+def _permutation(n: int, gen: torch.Generator) -> List[int]:
+    return torch.randperm(n, generator=gen).tolist()
+
+
+def _tables_tensor(tables: List[List[int]]) -> torch.Tensor:
+    width = max([len(t) for t in tables] + [1])
+    out = torch.full((len(tables), width), -1, dtype=torch.int32)
+    for s, t in enumerate(tables):
+        if t:
+            out[s, : len(t)] = torch.tensor(t, dtype=torch.int32)
+    return out
+
+
+def _decode_step_structure(ctx: List[int], block_size: int, num_blocks: int, gen: torch.Generator):
+    """Tables for sequences whose first ctx-1 tokens are cached, plus the slot
+    of each sequence's new token (position ctx-1).  Sequences with ctx = 0
+    have no token to write."""
+    mgr = BlockManager(num_blocks, block_size, _permutation(num_blocks, gen))
+    history_slots, new_slots = [], []
+    for s, n in enumerate(ctx):
+        mgr.add_sequence(s, max(n - 1, 0))
+        history_slots.extend(mgr.prompt_slots(s))
+        if n > 0:
+            new_slots.append(mgr.append_token(s))
+    tables = [mgr.table(s) for s in range(len(ctx))]
+    return tables, history_slots, new_slots
+
+
+# ---------------------------------------------------------------------------
+# payloads
+# ---------------------------------------------------------------------------
+def _normal(shape, dtype, gen, device) -> torch.Tensor:
+    return torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(dtype)
+
+
+def _pool_from_tokens(tokens: torch.Tensor, slots: List[int], num_blocks: int, block_size: int) -> torch.Tensor:
+    """Pool [NB][Hkv][B][d] holding token i's rows at slot slots[i], NaN elsewhere."""
+    t, hkv, d = tokens.shape
+    flat = torch.full((num_blocks * block_size, hkv, d), float("nan"), dtype=tokens.dtype,
+                      device=tokens.device)
+    if t:
+        index = torch.tensor(slots, dtype=torch.int64, device=tokens.device)
+        flat.index_copy_(0, index, tokens)
+    return flat.view(num_blocks, block_size, hkv, d).permute(0, 2, 1, 3).contiguous()
+
+
+def _assemble(name, ctx, tables, history_slots, new_slots, copy_pairs, *, num_heads, num_kv_heads,
+              head_dim, block_size, dtype, num_blocks, partition_size, seed, device, notes=None):
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    n_hist = len(history_slots)
+    keys = _normal((n_hist, num_kv_heads, head_dim), dtype, gen, device)
+    values = _normal((n_hist, num_kv_heads, head_dim), dtype, gen, device)
+    k_cache = _pool_from_tokens(keys, history_slots, num_blocks, block_size)
+    del keys
+    v_cache = _pool_from_tokens(values, history_slots, num_blocks, block_size)
+    del values
+    s = len(ctx)
+    query = _normal((s, num_heads, head_dim), dtype, gen, device)
+    t = len(new_slots)
+    new_key = _normal((t, num_kv_heads, head_dim), dtype, gen, device)
+    new_value = _normal((t, num_kv_heads, head_dim), dtype, gen, device)
+    return Workload(
+        name=name, num_seqs=s, num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+        block_size=block_size, dtype=dtype, num_blocks=num_blocks,
+        scale=1.0 / math.sqrt(head_dim), partition_size=partition_size,
+        context_lens=torch.tensor(ctx, dtype=torch.int32, device=device),
+        block_tables=_tables_tensor(tables).to(device),
+        query=query, k_cache=k_cache, v_cache=v_cache, new_key=new_key, new_value=new_value,
+        slot_mapping=torch.tensor(new_slots, dtype=torch.int64, device=device),
+        copy_pairs=torch.tensor(copy_pairs, dtype=torch.int64, device=device).reshape(-1, 2),
+        seed=seed, notes=dict(notes or {}))
+
+
+# ---------------------------------------------------------------------------
+# the five workloads
+# ---------------------------------------------------------------------------
+def _simple(name, ctx, *, num_heads, num_kv_heads, head_dim, block_size, dtype, num_blocks,
+            partition_size, seed, device, gen_cpu, notes=None):
+    tables, hist, new = _decode_step_structure(ctx, block_size, num_blocks, gen_cpu)
+    return _assemble(name, ctx, tables, hist, new, [], num_heads=num_heads,
+                     num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=block_size,
+                     dtype=dtype, num_blocks=num_blocks, partition_size=partition_size,
+                     seed=seed, device=device, notes=notes)
+
+
+def custom(ctx: List[int], *, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+           dtype: torch.dtype, num_blocks: Optional[int] = None, partition_size: int = 0,
+           seed: int = SEED_BASE + 99, device="cpu", name="custom") -> Workload:
+    """A decode step over arbitrary context lengths (edge cases, sweeps).
+    The pool defaults to exactly the blocks needed, in a shuffled order."""
+    gen_cpu = torch.Generator().manual_seed(seed)
+    needed = sum(blocks_needed(n, block_size) for n in ctx)
+    nb = max(num_blocks if num_blocks is not None else needed, 1)
+    return _simple(name, list(ctx), num_heads=num_heads, num_kv_heads=num_kv_heads,
+                   head_dim=head_dim, block_size=block_size, dtype=dtype, num_blocks=nb,
+                   partition_size=partition_size, seed=seed, device=device, gen_cpu=gen_cpu)
+
+
+def make(name: str, device="cpu", *, block_size: Optional[int] = None, num_seqs: Optional[int] = None,
+         seed: Optional[int] = None) -> Workload:
+    """Build workload ``name`` (see the module docstring).  ``num_seqs`` keeps
+    only the first n sequences (a smaller case with the same distribution);
+    ``block_size`` selects the long_context sweep point."""
+    if name not in _INDEX:
+        raise KeyError(f"unknown workload {name!r}; choose from {WORKLOADS}")
+    seed = SEED_BASE + _INDEX[name] if seed is None else seed
+    gen_cpu = torch.Generator().manual_seed(seed)
+
+    if name == "tiny":
+        ctx = [5, 17, 33, 64][: num_seqs or 4]
+        return _simple(name, ctx, num_heads=4, num_kv_heads=4, head_dim=64, block_size=16,
+                       dtype=torch.float32, num_blocks=32, partition_size=0, seed=seed,
+                       device=device, gen_cpu=gen_cpu)
+
+    if name == "opt13b":
+        s = 64
+        ctx = torch.randint(128, 2049, (s,), generator=gen_cpu).tolist()[: num_seqs or s]
+        needed = sum(blocks_needed(n, 16) for n in ctx)
+        return _simple(name, ctx, num_heads=40, num_kv_heads=40, head_dim=128, block_size=16,
+                       dtype=torch.float16, num_blocks=math.ceil(1.1 * needed), partition_size=0,
+                       seed=seed, device=device, gen_cpu=gen_cpu)
+
+    if name == "llama8b":
+        s = 256
+        draw = torch.empty(s, dtype=torch.float64).log_normal_(math.log(1024.0), 1.0, generator=gen_cpu)
+        ctx = torch.clamp(torch.round(draw), 16, 8192).to(torch.int64).tolist()[: num_seqs or s]
+        needed = sum(blocks_needed(n, 16) for n in ctx)
+        return _simple(name, ctx, num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                       dtype=torch.bfloat16, num_blocks=needed, partition_size=0, seed=seed,
+                       device=device, gen_cpu=gen_cpu,
+                       notes={"lognormal": "mu=ln(1024), sigma=1.0, rounded, clipped to [16,8192]"})
+
+    if name == "long_context":
+        bs = block_size or 16
+        if bs not in (8, 16, 32):
+            raise ValueError("long_context sweeps block sizes 8, 16 and 32")
+        s = num_seqs or 16
+        ctx = [32768] * s
+        # The token payload depends only on the seed, not on the block size,
+        # so the three sweep points hold the same batch.
+        needed = sum(blocks_needed(n, bs) for n in ctx)
+        tables, hist, new = _decode_step_structure(ctx, bs, needed, gen_cpu)
+        return _assemble(name, ctx, tables, hist, new, [], num_heads=32, num_kv_heads=8,
+                         head_dim=128, block_size=bs, dtype=torch.bfloat16, num_blocks=needed,
+                         partition_size=512, seed=seed, device=device)
+
+    # parallel_sampling
+    prompts, samples, prompt_len, bs = 32, 8, 1000, 16
+    if num_seqs is not None:
+        prompts = max(1, num_seqs // samples)
+    tails = torch.randint(0, 513, (prompts * samples,), generator=gen_cpu).tolist()
+
+    def simulate(num_blocks, free_order):
+        mgr = BlockManager(num_blocks, bs, free_order)
+        hist = []
+        for p in range(prompts):
+            base = p * samples
+            mgr.add_sequence(base, prompt_len)
+            hist.extend(mgr.prompt_slots(base))
+            for i in range(1, samples):
+                mgr.fork(base, base + i)
+        new = []
+        for seq in range(prompts * samples):
+            for _ in range(tails[seq] + 1):  # the tail, then this step's token
+                new.append(mgr.append_token(seq))
+        used = num_blocks - mgr.num_free()
+        return mgr, hist, new, used
+
+    bound = prompts * samples * (blocks_needed(prompt_len + 513, bs) + 1)
+    _, _, _, used = simulate(bound, None)
+    nb = math.ceil(1.1 * used)
+    mgr, hist, new, _ = simulate(nb, _permutation(nb, gen_cpu))
+    pairs = mgr.take_copies()
+    ctx = [prompt_len + tails[q] + 1 for q in range(prompts * samples)]
+    tables = [mgr.table(q) for q in range(prompts * samples)]
+    return _assemble(name, ctx, tables, hist, new, pairs, num_heads=32, num_kv_heads=8,
+                     head_dim=128, block_size=bs, dtype=torch.bfloat16, num_blocks=nb,
+                     partition_size=0, seed=seed, device=device,
+                     notes={"prompts": prompts, "samples": samples, "prompt_len": prompt_len,
+                            "unique_blocks_used": used})
