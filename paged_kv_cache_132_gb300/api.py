@@ -1,0 +1,133 @@
+"""Python binding of the C ABI: argument marshalling only.
+
+Every function takes CUDA tensors, checks their shapes and dtypes, and calls
+the same-named entry point of ``libpa.so`` on the current (or given) stream.
+All computation happens in the library's kernels; nothing here falls back to
+PyTorch or the CPU.  PyTorch provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+from . import native
+from .native import CacheDesc, PaError
+
+DTYPE_CODE = {torch.float32: native.PA_F32, torch.float16: native.PA_F16, torch.bfloat16: native.PA_BF16}
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _require(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _check_cuda(*tensors: torch.Tensor) -> None:
+    for t in tensors:
+        _require(t.is_cuda, "tensors must be on a CUDA device")
+        _require(t.is_contiguous(), "tensors must be contiguous")
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    _require(k_cache.dim() == 4, "a pool is [num_blocks][num_kv_heads][block_size][head_dim]")
+    _require(k_cache.dtype in DTYPE_CODE, f"unsupported cache dtype {k_cache.dtype}")
+    nb, hkv, bs, d = k_cache.shape
+    return CacheDesc(nb, hkv, bs, d, DTYPE_CODE[k_cache.dtype])
+
+
+def _raise(status: int, what: str) -> None:
+    if status != native.PA_OK:
+        raise PaError(status, what)
+
+
+def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      slot_mapping: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Write key/value [T][Hkv][d] into the pools at slot_mapping[t] (< 0: skip)."""
+    lib = native.load()
+    _check_cuda(key, value, k_cache, v_cache, slot_mapping)
+    _require(k_cache.shape == v_cache.shape and k_cache.dtype == v_cache.dtype, "K and V pools must match")
+    _require(key.dtype == k_cache.dtype and value.dtype == k_cache.dtype, "key/value dtype must match the pools")
+    _require(key.dim() == 3 and key.shape == value.shape, "key/value are [num_tokens][num_kv_heads][head_dim]")
+    _require(tuple(key.shape[1:]) == (k_cache.shape[1], k_cache.shape[3]), "key/value heads or head_dim mismatch")
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == key.shape[0], "slot_mapping is int64 [T]")
+    desc = cache_desc(k_cache)
+    _raise(lib.pa_reshape_and_cache(key.data_ptr(), value.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                    slot_mapping.data_ptr(), key.shape[0], ctypes.byref(desc),
+                                    _stream_ptr(stream)), "pa_reshape_and_cache")
+
+
+def decode_workspace_size(num_seqs: int, num_heads: int, max_context_len: int, partition_size: int = 0,
+                          head_dim: int = 128) -> int:
+    return int(native.load().pa_decode_workspace_size(num_seqs, num_heads, max_context_len, partition_size,
+                                                      head_dim))
+
+
+def decode(query: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+           context_lens: torch.Tensor, scale: float, *, num_kv_heads: Optional[int] = None,
+           out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.float32,
+           max_context_len: Optional[int] = None, partition_size: int = 0,
+           workspace: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Paged decode attention; returns out [S][H][d].
+
+    ``max_context_len`` is a host-side upper bound of context_lens; when None
+    the table capacity (max_blocks_per_seq * block_size) is used, which needs
+    no device sync but may size a larger workspace."""
+    lib = native.load()
+    _check_cuda(query, k_cache, v_cache, block_tables, context_lens)
+    _require(query.dim() == 3, "query is [num_seqs][num_heads][head_dim]")
+    s, h, d = query.shape
+    desc = cache_desc(k_cache)
+    _require(k_cache.shape == v_cache.shape and v_cache.dtype == k_cache.dtype, "K and V pools must match")
+    _require(query.dtype == k_cache.dtype and d == desc.head_dim, "query dtype/head_dim must match the pools")
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == s,
+             "block_tables is int32 [num_seqs][max_blocks]")
+    _require(context_lens.dtype == torch.int32 and context_lens.numel() == s, "context_lens is int32 [num_seqs]")
+    hkv = desc.num_kv_heads if num_kv_heads is None else num_kv_heads
+    max_blocks = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = max_blocks * desc.block_size
+    if out is None:
+        out = torch.empty((s, h, d), dtype=out_dtype, device=query.device)
+    _check_cuda(out)
+    _require(out.shape == (s, h, d) and out.dtype in DTYPE_CODE, "out is [num_seqs][num_heads][head_dim]")
+    need = decode_workspace_size(s, h, max_context_len, partition_size, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=query.device)
+    _check_cuda(workspace)
+    _raise(lib.pa_decode(out.data_ptr(), DTYPE_CODE[out.dtype], query.data_ptr(), k_cache.data_ptr(),
+                         v_cache.data_ptr(), ctypes.byref(desc), block_tables.data_ptr(), max_blocks,
+                         context_lens.data_ptr(), s, int(max_context_len), h, hkv, float(scale),
+                         int(partition_size), workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)),
+           "pa_decode")
+    return out
+
+
+def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor], src_dst_pairs: torch.Tensor,
+                stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy-on-write: copy K and V block pairs[i][0] -> pairs[i][1] in every layer."""
+    lib = native.load()
+    _require(len(k_caches) == len(v_caches) and len(k_caches) > 0, "one K and one V pool per layer")
+    _check_cuda(*k_caches, *v_caches, src_dst_pairs)
+    _require(src_dst_pairs.dtype == torch.int64 and src_dst_pairs.dim() == 2 and src_dst_pairs.shape[1] == 2,
+             "src_dst_pairs is int64 [n][2]")
+    desc = cache_desc(k_caches[0])
+    for p in list(k_caches) + list(v_caches):
+        _require(p.shape == k_caches[0].shape and p.dtype == k_caches[0].dtype, "all pools must match")
+    n = len(k_caches)
+    kp = (ctypes.c_void_p * n)(*[p.data_ptr() for p in k_caches])
+    vp = (ctypes.c_void_p * n)(*[p.data_ptr() for p in v_caches])
+    _raise(lib.pa_copy_blocks(kp, vp, n, src_dst_pairs.data_ptr(), src_dst_pairs.shape[0], ctypes.byref(desc),
+                              _stream_ptr(stream)), "pa_copy_blocks")
+
+
+def get_device_error(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:
+    """(status, PA_DEVERR_* mask); synchronises the stream and clears the word."""
+    code = ctypes.c_int32(0)
+    status = native.load().pa_get_device_error(_stream_ptr(stream), ctypes.byref(code))
+    return int(status), int(code.value)

@@ -1,0 +1,127 @@
+// cache_ops.cu -- the two kernels that maintain the paged KV cache.
+//
+//  * reshape_and_cache: "fused reshape and block write" ("Efficient Memory
+//    Management for Large Language Model Serving with PagedAttention Review",
+//    §3-2).  Each new token's K and V rows go straight from the projection
+//    layout [T][Hkv][d] into their slot of the block layout
+//    [NB][Hkv][B][d] in one pass, 16 bytes per thread, so that consecutive
+//    threads read consecutive bytes of the source and write whole rows of
+//    the destination.
+//  * copy_blocks: "fused block copy for copy-on-write" (same page, §3-2;
+//    "PagedAttention 论文精读笔记", §6.1).  One launch copies every (pair,
+//    layer, K|V) block, one CTA per block, each thread keeping several
+//    16-byte loads in flight before its stores.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pa {
+namespace {
+
+constexpr int kWriteThreads = 256;
+
+__global__ void __launch_bounds__(kWriteThreads)
+reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                         uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                         const int64_t* __restrict__ slot_mapping, int64_t num_tokens, int num_kv_heads,
+                         int block_size, int chunks_per_row, int64_t num_slots, int* err) {
+    // Thread index -> (token t, K|V, head h, 16-byte chunk c), chunk fastest.
+    const int64_t total = num_tokens * 2 * num_kv_heads * chunks_per_row;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+        const int c = (int)(idx % chunks_per_row);
+        int64_t rest = idx / chunks_per_row;
+        const int h = (int)(rest % num_kv_heads);
+        rest /= num_kv_heads;
+        const int is_value = (int)(rest & 1);
+        const int64_t t = rest >> 1;
+        const int64_t slot = __ldg(slot_mapping + t);
+        if (slot < 0) continue;  // padding token: nothing to store
+        if (slot >= num_slots) {
+            if (h == 0 && c == 0 && !is_value) set_error(err, PA_DEVERR_SLOT);
+            continue;
+        }
+        const int64_t block = slot / block_size;
+        const int64_t offset = slot - block * block_size;
+        const uint4* src = (is_value ? value : key) + ((t * num_kv_heads + h) * chunks_per_row + c);
+        uint4* dst = (is_value ? v_cache : k_cache) +
+                     (((block * num_kv_heads + h) * block_size + offset) * chunks_per_row + c);
+        *dst = __ldg(src);
+    }
+}
+
+struct CopyPools {
+    uint4* k[kMaxCopyLayers];
+    uint4* v[kMaxCopyLayers];
+};
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 8;
+
+__global__ void __launch_bounds__(kCopyThreads)
+copy_blocks_kernel(const __grid_constant__ CopyPools pools, int num_layers, const int64_t* __restrict__ pairs,
+                   int64_t num_blocks, int64_t vecs_per_block, int* err) {
+    // blockIdx.x -> (pair, layer, K|V), K|V fastest.
+    const int64_t id = blockIdx.x;
+    const int is_value = (int)(id & 1);
+    const int layer = (int)((id >> 1) % num_layers);
+    const int64_t pair = (id >> 1) / num_layers;
+    const int64_t src = __ldg(pairs + 2 * pair);
+    const int64_t dst = __ldg(pairs + 2 * pair + 1);
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (threadIdx.x == 0 && layer == 0 && !is_value) set_error(err, PA_DEVERR_COPY_PAIR);
+        return;
+    }
+    uint4* base = is_value ? pools.v[layer] : pools.k[layer];
+    const uint4* from = base + src * vecs_per_block;
+    uint4* to = base + dst * vecs_per_block;
+    for (int64_t i0 = threadIdx.x; i0 < vecs_per_block; i0 += (int64_t)kCopyThreads * kCopyUnroll) {
+        uint4 buf[kCopyUnroll];
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+            const int64_t i = i0 + (int64_t)u * kCopyThreads;
+            if (i < vecs_per_block) buf[u] = __ldcs(from + i);
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+            const int64_t i = i0 + (int64_t)u * kCopyThreads;
+            if (i < vecs_per_block) to[i] = buf[u];
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                                     const int64_t* slot_mapping, int64_t num_tokens,
+                                     const PoolShape& shape, int* err, cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int chunks = shape.head_dim * shape.elem_bytes / 16;
+    const int64_t total = num_tokens * 2 * shape.num_kv_heads * chunks;
+    int64_t blocks = (total + kWriteThreads - 1) / kWriteThreads;
+    if (blocks > 65536) blocks = 65536;  // grid-stride beyond this
+    reshape_and_cache_kernel<<<(unsigned)blocks, kWriteThreads, 0, stream>>>(
+        static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
+        static_cast<uint4*>(v_cache), slot_mapping, num_tokens, shape.num_kv_heads, shape.block_size, chunks,
+        shape.num_blocks * shape.block_size, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
+                               const int64_t* pairs, int64_t num_pairs, const PoolShape& shape,
+                               int* err, cudaStream_t stream) {
+    if (num_pairs == 0) return cudaSuccess;
+    CopyPools pools{};
+    for (int l = 0; l < num_layers; ++l) {
+        pools.k[l] = static_cast<uint4*>(k_caches[l]);
+        pools.v[l] = static_cast<uint4*>(v_caches[l]);
+    }
+    const int64_t block_bytes =
+        (int64_t)shape.num_kv_heads * shape.block_size * shape.head_dim * shape.elem_bytes;
+    const int64_t ctas = num_pairs * num_layers * 2;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    copy_blocks_kernel<<<(unsigned)ctas, kCopyThreads, 0, stream>>>(pools, num_layers, pairs, shape.num_blocks,
+                                                                     block_bytes / 16, err);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,74 @@
+// kernels.h -- internal interface between the C ABI (pa_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace pa {
+
+struct PoolShape {
+    int64_t num_blocks;
+    int num_kv_heads;
+    int block_size;
+    int head_dim;
+    int elem_bytes;
+};
+
+// ---- cache write / block copy (cache_ops.cu) --------------------------------
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                                     const int64_t* slot_mapping, int64_t num_tokens,
+                                     const PoolShape& shape, int* err, cudaStream_t stream);
+
+constexpr int kMaxCopyLayers = 256;
+cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
+                               const int64_t* pairs, int64_t num_pairs, const PoolShape& shape,
+                               int* err, cudaStream_t stream);
+
+// ---- decode (decode_*.cu) ----------------------------------------------------
+// Everything one decode launch needs; passed by value as the kernel argument.
+struct DecodeParams {
+    void* out;
+    int out_dtype;
+    const void* query;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    int max_blocks;            // block table row length
+    const int32_t* context_lens;
+    int num_seqs;
+    int num_heads;
+    int num_kv_heads;
+    int64_t num_blocks;
+    float scale_log2;          // scale * log2(e): scores are kept in base-2 units
+    int partition_size;        // tokens per split-KV partition (multiple of the stage)
+    int max_parts;             // partitions per sequence the workspace holds
+    int ctx_cap;               // min(max_blocks * block_size, max_parts * partition_size)
+    // workspace views
+    int* next_item;            // dynamic work counter
+    int* num_items;            // (sequence, partition) pairs x num_kv_heads
+    int2* items;               // (sequence, partition) pairs
+    int* counters;             // [num_seqs * num_kv_heads] partitions finished
+    float* part_ml;            // [num_seqs * num_kv_heads * max_parts * G][2] (max, sum)
+    float* part_o;             // [num_seqs * num_kv_heads * max_parts * G][head_dim]
+    int* err;                  // device error word
+    unsigned long long wait_limit_ns;
+};
+
+struct DecodeWorkspaceLayout {
+    size_t next_item, num_items, items, counters, part_ml, part_o, total;
+};
+
+DecodeWorkspaceLayout decode_workspace_layout(int num_seqs, int num_heads, int max_parts, int head_dim);
+
+// Tokens per pipeline stage of the decode kernel for this head_dim/element
+// size; partition sizes are multiples of it.
+int decode_stage_tokens(int head_dim, int elem_bytes);
+
+// Launch the planning kernel and the decode kernel on `stream`.
+// Returns cudaErrorNotSupported when no kernel exists for the shape.
+cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int block_size, int group,
+                          int grid_items_upper_bound, cudaStream_t stream);
+
+}  // namespace pa

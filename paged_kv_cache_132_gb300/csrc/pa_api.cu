@@ -1,0 +1,260 @@
+// pa_api.cu -- the C ABI declared in include/pa.h: argument checks, the
+// per-device error word, the partition choice, and the launches.
+//
+// Every argument error is caught here, before anything reaches the GPU; the
+// kernels only report what depends on device data (ids, slots, lengths) or on
+// time (a bounded wait that ran out), through the error word.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/pa.h"
+#include "kernels.h"
+
+namespace {
+
+// One error word per device (a __device__ variable exists once per device
+// that loads the library); read and cleared by pa_get_device_error.
+__device__ int g_device_error;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+int* g_error_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+constexpr int kAutoPartitionSmall = 256;
+constexpr int kAutoPartition = 512;
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+int* error_word(int dev) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_error_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        g_error_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_error_ptr[dev];
+}
+
+int sm_count(int dev) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+// Wall-time limit of every wait inside a kernel (environment variable
+// PA_WAIT_TIMEOUT_MS, default 2000 ms).
+unsigned long long wait_limit_ns() {
+    static const unsigned long long limit = [] {
+        const char* s = std::getenv("PA_WAIT_TIMEOUT_MS");
+        long long ms = s ? std::atoll(s) : 2000;
+        if (ms <= 0) ms = 2000;
+        return (unsigned long long)ms * 1000000ull;
+    }();
+    return limit;
+}
+
+int elem_bytes(int dtype) {
+    switch (dtype) {
+        case PA_F32: return 4;
+        case PA_F16:
+        case PA_BF16: return 2;
+        default: return 0;
+    }
+}
+
+bool aligned(const void* p, uintptr_t a) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_cache(const pa_cache_desc* c, pa::PoolShape* shape) {
+    if (!c) return PA_ERR_INVALID_ARG;
+    const int eb = elem_bytes(c->dtype);
+    if (c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->block_size <= 0 || c->head_dim <= 0 || eb == 0)
+        return PA_ERR_INVALID_ARG;
+    if (((int64_t)c->head_dim * eb) % 16 != 0) return PA_ERR_INVALID_ARG;
+    shape->num_blocks = c->num_blocks;
+    shape->num_kv_heads = c->num_kv_heads;
+    shape->block_size = c->block_size;
+    shape->head_dim = c->head_dim;
+    shape->elem_bytes = eb;
+    return PA_OK;
+}
+
+int max_parts_for(int max_context_len, int partition) {
+    const int parts = (max_context_len + partition - 1) / partition;
+    return parts < 1 ? 1 : parts;
+}
+
+bool partition_ok(int32_t partition_size) { return partition_size == 0 || (partition_size > 0 && partition_size % 64 == 0); }
+
+int status_of(cudaError_t e) {
+    if (e == cudaSuccess) return PA_OK;
+    if (e == cudaErrorNotSupported) return PA_ERR_UNSUPPORTED;
+    return PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_abi_version(void) { return PA_ABI_VERSION; }
+
+const char* pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_DEVICE_FAULT: return "PA_ERR_DEVICE_FAULT";
+        case PA_ERR_DEVICE_TIMEOUT: return "PA_ERR_DEVICE_TIMEOUT";
+        default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int64_t num_tokens, const pa_cache_desc* cache,
+                         void* stream) {
+    pa::PoolShape shape;
+    int rc = check_cache(cache, &shape);
+    if (rc != PA_OK) return rc;
+    if (num_tokens < 0) return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return PA_ERR_INVALID_ARG;
+    const int dev = current_device();
+    if (dev < 0) return PA_ERR_CUDA;
+    int* err = error_word(dev);
+    if (!err) return PA_ERR_CUDA;
+    return status_of(pa::launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens, shape,
+                                                  err, static_cast<cudaStream_t>(stream)));
+}
+
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t max_context_len,
+                                int32_t partition_size, int32_t head_dim) {
+    if (num_seqs < 0 || num_heads <= 0 || max_context_len < 0 || head_dim <= 0 || !partition_ok(partition_size))
+        return 0;
+    const int part = partition_size ? partition_size : kAutoPartitionSmall;
+    return pa::decode_workspace_layout(num_seqs, num_heads, max_parts_for(max_context_len, part), head_dim).total;
+}
+
+int pa_decode(void* out, int32_t out_dtype, const void* query, const void* k_cache, const void* v_cache,
+              const pa_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+              const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len, int32_t num_heads,
+              int32_t num_kv_heads, float scale, int32_t partition_size, void* workspace,
+              size_t workspace_bytes, void* stream) {
+    pa::PoolShape shape;
+    int rc = check_cache(cache, &shape);
+    if (rc != PA_OK) return rc;
+    if (elem_bytes(out_dtype) == 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads != cache->num_kv_heads || num_heads % num_kv_heads != 0 ||
+        max_blocks_per_seq <= 0 || max_context_len < 0 || !std::isfinite(scale) || !partition_ok(partition_size))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!aligned(out, 16) || !aligned(query, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    const int group = num_heads / num_kv_heads;
+    if (!(group == 1 || group == 2 || group == 4 || group == 8)) return PA_ERR_UNSUPPORTED;
+    if (!(shape.head_dim == 64 || shape.head_dim == 128)) return PA_ERR_UNSUPPORTED;
+    if (!(shape.block_size == 8 || shape.block_size == 16 || shape.block_size == 32)) return PA_ERR_UNSUPPORTED;
+
+    const int dev = current_device();
+    if (dev < 0) return PA_ERR_CUDA;
+    int* err = error_word(dev);
+    const int sms = sm_count(dev);
+    if (!err || sms <= 0) return PA_ERR_CUDA;
+
+    int part = partition_size;
+    if (part == 0) {
+        // Enough independent (sequence, KV head, partition) items to keep
+        // every SM busy through the tail; shorter partitions when the batch
+        // is small.
+        const int64_t units = (int64_t)num_seqs * num_kv_heads;
+        part = units * max_parts_for(max_context_len, kAutoPartition) < 4LL * sms ? kAutoPartitionSmall
+                                                                                  : kAutoPartition;
+    }
+    const int max_parts = max_parts_for(max_context_len, part);
+    const pa::DecodeWorkspaceLayout lay = pa::decode_workspace_layout(num_seqs, num_heads, max_parts, shape.head_dim);
+    if (!aligned(workspace, 256) || workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
+    const int64_t items_ub = (int64_t)num_seqs * max_parts * num_kv_heads;
+    if (items_ub > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+
+    char* ws = static_cast<char*>(workspace);
+    pa::DecodeParams p{};
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.query = query;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.max_blocks = max_blocks_per_seq;
+    p.context_lens = context_lens;
+    p.num_seqs = num_seqs;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.num_blocks = shape.num_blocks;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.partition_size = part;
+    p.max_parts = max_parts;
+    const int64_t table_cap = (int64_t)max_blocks_per_seq * shape.block_size;
+    const int64_t part_cap = (int64_t)max_parts * part;
+    const int64_t cap = table_cap < part_cap ? table_cap : part_cap;
+    p.ctx_cap = (int)(cap < 0x7fffffffLL ? cap : 0x7fffffffLL);
+    p.next_item = reinterpret_cast<int*>(ws + lay.next_item);
+    p.num_items = reinterpret_cast<int*>(ws + lay.num_items);
+    p.items = reinterpret_cast<int2*>(ws + lay.items);
+    p.counters = reinterpret_cast<int*>(ws + lay.counters);
+    p.part_ml = reinterpret_cast<float*>(ws + lay.part_ml);
+    p.part_o = reinterpret_cast<float*>(ws + lay.part_o);
+    p.err = err;
+    p.wait_limit_ns = wait_limit_ns();
+    return status_of(pa::launch_decode(p, cache->dtype, shape.head_dim, shape.block_size, group, (int)items_ub,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers, const int64_t* src_dst_pairs,
+                   int64_t num_pairs, const pa_cache_desc* cache, void* stream) {
+    pa::PoolShape shape;
+    int rc = check_cache(cache, &shape);
+    if (rc != PA_OK) return rc;
+    if (num_layers < 1 || num_layers > pa::kMaxCopyLayers || num_pairs < 0 || !k_caches || !v_caches)
+        return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!aligned(src_dst_pairs, 8)) return PA_ERR_INVALID_ARG;
+    for (int l = 0; l < num_layers; ++l)
+        if (!aligned(k_caches[l], 16) || !aligned(v_caches[l], 16)) return PA_ERR_INVALID_ARG;
+    const int dev = current_device();
+    if (dev < 0) return PA_ERR_CUDA;
+    int* err = error_word(dev);
+    if (!err) return PA_ERR_CUDA;
+    return status_of(pa::launch_copy_blocks(k_caches, v_caches, num_layers, src_dst_pairs, num_pairs, shape, err,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+int pa_get_device_error(void* stream, int32_t* code) {
+    if (!code) return PA_ERR_INVALID_ARG;
+    *code = 0;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_device_error, sizeof(int)) != cudaSuccess) return PA_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return PA_ERR_CUDA;
+    *code = word;
+    if (word == 0) return PA_OK;
+    return (word & PA_DEVERR_TIMEOUT) ? PA_ERR_DEVICE_TIMEOUT : PA_ERR_DEVICE_FAULT;
+}
+
+}  // extern "C"

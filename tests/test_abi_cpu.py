@@ -1,0 +1,113 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+and rejects bad arguments on the host before any CUDA call (CPU only)."""
+import ctypes
+
+import pytest
+
+from paged_kv_cache_132_gb300 import build, native
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return native.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = native.declared_symbols()
+    assert set(names) >= {"pa_reshape_and_cache", "pa_decode", "pa_copy_blocks", "pa_decode_workspace_size",
+                          "pa_get_device_error", "pa_status_string", "pa_abi_version"}
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in include/pa.h but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.pa_abi_version() == 1
+    for code, name in native.STATUS_NAMES.items():
+        assert lib.pa_status_string(code).decode() == name
+    assert lib.pa_status_string(-99).decode() == "PA_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    ws = lib.pa_decode_workspace_size
+    assert ws(4, 4, 64, 0, 64) > 0
+    # grows with the number of partitions
+    assert ws(16, 32, 32768, 512, 128) > ws(16, 32, 512, 512, 128)
+    # at least the partial outputs: S * H * parts * d floats
+    assert ws(16, 32, 32768, 512, 128) >= 16 * 32 * 64 * 128 * 4
+    # invalid arguments -> 0
+    assert ws(-1, 4, 64, 0, 64) == 0
+    assert ws(4, 0, 64, 0, 64) == 0
+    assert ws(4, 4, 64, 100, 64) == 0   # partition not a multiple of 64
+    assert ws(4, 4, -5, 0, 64) == 0
+
+
+FAKE = 0x10000  # aligned, never dereferenced: every case below fails validation first
+
+
+def _desc(nb=8, hkv=2, bs=16, d=64, dtype=native.PA_BF16):
+    return native.CacheDesc(nb, hkv, bs, d, dtype)
+
+
+def _decode(lib, **over):
+    a = dict(out=FAKE, out_dtype=native.PA_F32, query=FAKE, k=FAKE, v=FAKE, desc=_desc(), tables=FAKE,
+             max_blocks=4, ctx=FAKE, num_seqs=2, max_ctx=64, num_heads=4, num_kv_heads=2, scale=0.125,
+             part=0, ws=FAKE, ws_bytes=0, stream=None)
+    a.update(over)
+    return lib.pa_decode(a["out"], a["out_dtype"], a["query"], a["k"], a["v"], ctypes.byref(a["desc"]),
+                         a["tables"], a["max_blocks"], a["ctx"], a["num_seqs"], a["max_ctx"], a["num_heads"],
+                         a["num_kv_heads"], a["scale"], a["part"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(desc=_desc(nb=0)), -1),
+    (dict(desc=_desc(dtype=7)), -1),
+    (dict(desc=_desc(d=60)), -1),              # 120 bytes: not a multiple of 16
+    (dict(out_dtype=5), -1),
+    (dict(num_kv_heads=3), -1),                # differs from the pool
+    (dict(num_heads=5), -1),                   # not a multiple of num_kv_heads
+    (dict(query=FAKE + 8), -1),                # misaligned
+    (dict(out=0), -1),
+    (dict(tables=FAKE + 2), -1),
+    (dict(part=96), -1),
+    (dict(scale=float("nan")), -1),
+    (dict(max_blocks=0), -1),
+    (dict(num_heads=32, num_kv_heads=2), -2),  # group 16
+    (dict(desc=_desc(d=96)), -2),
+    (dict(desc=_desc(bs=64)), -2),
+    (dict(desc=_desc(bs=4)), -2),
+])
+def test_decode_rejects_on_host(lib, over, status):
+    assert _decode(lib, **over) == status
+
+
+def test_decode_empty_batch_is_noop(lib):
+    assert _decode(lib, num_seqs=0) == 0
+
+
+def test_reshape_and_cache_rejects_on_host(lib):
+    d = _desc()
+    f = lib.pa_reshape_and_cache
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, -1, ctypes.byref(d), None) == -1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 0, ctypes.byref(d), None) == 0     # no tokens: no-op
+    assert f(FAKE + 4, FAKE, FAKE, FAKE, FAKE, 3, ctypes.byref(d), None) == -1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE + 4, 3, ctypes.byref(d), None) == -1
+    bad = _desc(hkv=0)
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 3, ctypes.byref(bad), None) == -1
+
+
+def test_copy_blocks_rejects_on_host(lib):
+    d = _desc()
+    ptrs = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    f = lib.pa_copy_blocks
+    assert f(ptrs, ptrs, 0, FAKE, 3, ctypes.byref(d), None) == -1      # no layers
+    assert f(ptrs, ptrs, 257, FAKE, 3, ctypes.byref(d), None) == -1    # too many layers
+    assert f(ptrs, ptrs, 2, FAKE, -1, ctypes.byref(d), None) == -1
+    assert f(ptrs, ptrs, 2, FAKE, 0, ctypes.byref(d), None) == 0       # nothing to copy
+    assert f(ptrs, ptrs, 2, FAKE + 4, 3, ctypes.byref(d), None) == -1
+    mis = (ctypes.c_void_p * 2)(FAKE, FAKE + 8)
+    assert f(mis, ptrs, 2, FAKE, 3, ctypes.byref(d), None) == -1
+
+
+def test_get_device_error_needs_output(lib):
+    assert lib.pa_get_device_error(None, None) == -1
