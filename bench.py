@@ -166,7 +166,7 @@ def oracle_setup(w):
 
     def bits(t):
         t = t.detach().contiguous().cpu()
-        return t.numpy() if t.dtype == torch.float32 else t.view(torch.int16).numpy()
+        return t.view(torch.int32).numpy() if t.dtype == torch.float32 else t.view(torch.int16).numpy()
 
     orc = O.get()
     k = bits(w.k_cache).copy()

@@ -17,7 +17,7 @@ ATOL = 2e-3
 
 def bits(t: torch.Tensor) -> np.ndarray:
     t = t.detach().contiguous().cpu()
-    return t.numpy() if t.dtype == torch.float32 else t.view(torch.int16).numpy()
+    return t.view(torch.int32).numpy() if t.dtype == torch.float32 else t.view(torch.int16).numpy()
 
 
 def gpu_step(w, *, partition_size=None, out_dtype=torch.float32, max_context_len=None):

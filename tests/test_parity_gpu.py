@@ -121,8 +121,8 @@ def test_shared_prefix_equals_private_copies():
     k_priv = torch.empty((used,) + tuple(w.k_cache.shape[1:]), dtype=w.dtype)
     v_priv = torch.empty_like(k_priv)
     new_tables = torch.full_like(tables, -1)
-    kt = torch.from_numpy(kref).view(w.dtype) if w.dtype != torch.float32 else torch.from_numpy(kref)
-    vt = torch.from_numpy(vref).view(w.dtype) if w.dtype != torch.float32 else torch.from_numpy(vref)
+    kt = torch.from_numpy(kref).view(w.dtype)
+    vt = torch.from_numpy(vref).view(w.dtype)
     nxt = 0
     for s in range(w.num_seqs):
         for j in range(tables.shape[1]):
