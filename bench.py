@@ -41,7 +41,7 @@ from paged_kv_cache_132_gb300 import api, metrics, native, workloads  # noqa: E4
 WORKLOAD = "llama8b"
 METRIC = "paged decode-attention KV GB/s (% of GB300 HBM peak); seq-decode-steps/s"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_llama8b_ncu.md")
-KERNEL_SOURCES = ["decode_simt.cuh", "decode.cu", "common.cuh"]
+KERNEL_SOURCES = ["decode_mma.cuh", "decode_common.cuh", "decode.cu", "common.cuh"]
 
 
 def parse_args():
@@ -52,6 +52,12 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle leg")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="first n sequences only (a smaller case of the same distribution, for profiling)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) leg")
+    ap.add_argument("--no-rows", action="store_true", help="skip the copy-on-write row timing")
+    ap.add_argument("--decode-kernel", choices=["default", "simt"], default="default",
+                    help="simt: time the CUDA-core decode kernel instead of the tensor-core one")
     return ap.parse_args()
 
 
@@ -247,7 +253,7 @@ def run_reference(args, rank, world):
 def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     native.load()
-    w = workloads.make(WORKLOAD, device="cuda", seed=workloads.SEED_BASE + 2 + 1000 * rank)
+    w = workloads.make(WORKLOAD, device="cuda", seed=workloads.SEED_BASE + 2 + 1000 * rank, num_seqs=args.num_seqs)
     decode_b, write_b = step_bytes(w)
     stream = torch.cuda.current_stream()
     out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.float32, device="cuda")
@@ -303,58 +309,61 @@ def run_ours(args, rank, world, local_rank):
     step_ms = all_reduce_max(total_ms / k, world)
     launches = k * 3  # cache write + planning kernel + decode kernel
 
-    # ---- end to end through the public API with host buffers -----------
-    host = {name: getattr(w, name).cpu().pin_memory() for name in
-            ("query", "new_key", "new_value", "slot_mapping", "block_tables", "context_lens")}
-    dev = {name: torch.empty_like(getattr(w, name)) for name in host}
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_host.numel() * out_host.element_size()
+    e2e_ms, h2d, d2h, launches_e2e = None, 0, 0, 0
+    if not args.no_e2e:
+        # ---- end to end through the public API with host buffers -----------
+        host = {name: getattr(w, name).cpu().pin_memory() for name in
+                ("query", "new_key", "new_value", "slot_mapping", "block_tables", "context_lens")}
+        dev = {name: torch.empty_like(getattr(w, name)) for name in host}
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
 
-    def e2e_step():
-        for name, t in host.items():
-            dev[name].copy_(t, non_blocking=True)
-        api.reshape_and_cache(dev["new_key"], dev["new_value"], w.k_cache, w.v_cache, dev["slot_mapping"])
-        api.decode(dev["query"], w.k_cache, w.v_cache, dev["block_tables"], dev["context_lens"], w.scale, out=out,
-                   max_context_len=max_ctx, workspace=ws)
-        out_host.copy_(out, non_blocking=True)
+        def e2e_step():
+            for name, t in host.items():
+                dev[name].copy_(t, non_blocking=True)
+            api.reshape_and_cache(dev["new_key"], dev["new_value"], w.k_cache, w.v_cache, dev["slot_mapping"])
+            api.decode(dev["query"], w.k_cache, w.v_cache, dev["block_tables"], dev["context_lens"], w.scale, out=out,
+                       max_context_len=max_ctx, workspace=ws)
+            out_host.copy_(out, non_blocking=True)
 
-    k_e2e = max(3, min(k, 500))
-    for _ in range(3):
-        e2e_step()
-    barrier(world)
-    torch.cuda.synchronize()
-    s2 = torch.cuda.Event(enable_timing=True)
-    e2 = torch.cuda.Event(enable_timing=True)
-    s2.record(stream)
-    for _ in range(k_e2e):
-        e2e_step()
-    e2.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = all_reduce_max(s2.elapsed_time(e2) / k_e2e, world)
-    launches_e2e = k_e2e * 3
+        k_e2e = max(3, min(k, 500))
+        for _ in range(3):
+            e2e_step()
+        barrier(world)
+        torch.cuda.synchronize()
+        s2 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = all_reduce_max(s2.elapsed_time(e2) / k_e2e, world)
+        launches_e2e = k_e2e * 3
 
-    # ---- rows not in this workload's step: copy-on-write copies ----------
     rows = {"a1_cache_write_us": 1e3 * write_ms, "a2_a6_decode_us": 1e3 * decode_ms}
-    ps = workloads.make("parallel_sampling", device="cuda")
-    ck, cv = ps.k_cache.clone(), ps.v_cache.clone()
-    for _ in range(5):
-        api.copy_blocks([ck], [cv], ps.copy_pairs)
-    torch.cuda.synchronize()
-    cs = torch.cuda.Event(enable_timing=True)
-    ce = torch.cuda.Event(enable_timing=True)
-    reps = 200
-    cs.record(stream)
-    for _ in range(reps):
-        api.copy_blocks([ck], [cv], ps.copy_pairs)
-    ce.record(stream)
-    torch.cuda.synchronize()
-    copy_us = 1e3 * cs.elapsed_time(ce) / reps
-    copy_b = metrics.copy_bytes(ps.copy_pairs.shape[0], 1, ps.num_kv_heads, ps.block_size, ps.head_dim, 2)
-    rows["a7_copy_blocks_us"] = copy_us
-    rows["a7_copy_blocks_gbs"] = copy_b / (copy_us * 1e-6) / 1e9
-    rows["a7_copy_blocks_pairs"] = int(ps.copy_pairs.shape[0])
-    del ps, ck, cv
+    if not args.no_rows:
+        # ---- rows not in this workload's step: copy-on-write copies ----------
+        ps = workloads.make("parallel_sampling", device="cuda")
+        ck, cv = ps.k_cache.clone(), ps.v_cache.clone()
+        for _ in range(5):
+            api.copy_blocks([ck], [cv], ps.copy_pairs)
+        torch.cuda.synchronize()
+        cs = torch.cuda.Event(enable_timing=True)
+        ce = torch.cuda.Event(enable_timing=True)
+        reps = 200
+        cs.record(stream)
+        for _ in range(reps):
+            api.copy_blocks([ck], [cv], ps.copy_pairs)
+        ce.record(stream)
+        torch.cuda.synchronize()
+        copy_us = 1e3 * cs.elapsed_time(ce) / reps
+        copy_b = metrics.copy_bytes(ps.copy_pairs.shape[0], 1, ps.num_kv_heads, ps.block_size, ps.head_dim, 2)
+        rows["a7_copy_blocks_us"] = copy_us
+        rows["a7_copy_blocks_gbs"] = copy_b / (copy_us * 1e-6) / 1e9
+        rows["a7_copy_blocks_pairs"] = int(ps.copy_pairs.shape[0])
+        del ps, ck, cv
 
     # ---- CPU oracle baseline (rank 0, one GPU only) ------------------------
     cpu = None
@@ -381,17 +390,19 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: 256 seqs, 32 query / 8 KV heads, d 128, bf16 K/V, block 16, "
+        "config": {"workload": f"{WORKLOAD}: {w.num_seqs} seqs, 32 query / 8 KV heads, d 128, bf16 K/V, block 16, "
                                f"lognormal ctx (median 1024, [16, 8192]), shuffled blocks",
                    "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (1.8 GB of KV per step)",
                    "algorithmic_bytes_per_step": bytes_step, "sum_context_tokens": int(w.context_lens.sum())},
         "seq_decode_steps_per_s": world * w.num_seqs / (step_ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": "pa_decode (planning + decode kernels), CUDA events per call"},
+                     "kernel": f"pa_decode ({'CUDA-core' if args.decode_kernel == 'simt' else 'tensor-core'} "
+                               f"decode kernel + planning kernel), CUDA events per call"},
         "rows": rows,
-        "e2e": {"value": world * bytes_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "e2e": None if e2e_ms is None else {
+            "value": world * bytes_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
         "gpu_launches_e2e": launches_e2e,
         "clocks": clocks,
@@ -403,6 +414,8 @@ def run_ours(args, rank, world, local_rank):
 
 def main():
     args = parse_args()
+    if args.decode_kernel == "simt":
+        os.environ["PA_DECODE_KERNEL"] = "simt"
     rank, world, local_rank = dist_env()
     if world > 1:
         import torch.distributed as dist

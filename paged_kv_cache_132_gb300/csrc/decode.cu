@@ -14,10 +14,14 @@ namespace pa {
 
 cudaError_t launch_decode_f32(const DecodeParams& p, int head_dim, int block_size, int group, int ub,
                               cudaStream_t stream);
-cudaError_t launch_decode_f16(const DecodeParams& p, int head_dim, int block_size, int group, int ub,
-                              cudaStream_t stream);
-cudaError_t launch_decode_bf16(const DecodeParams& p, int head_dim, int block_size, int group, int ub,
-                               cudaStream_t stream);
+cudaError_t launch_decode_simt_f16(const DecodeParams& p, int head_dim, int block_size, int group, int ub,
+                                  cudaStream_t stream);
+cudaError_t launch_decode_simt_bf16(const DecodeParams& p, int head_dim, int block_size, int group, int ub,
+                                   cudaStream_t stream);
+cudaError_t launch_decode_mma_f16(const DecodeParams& p, int head_dim, int block_size, int group, int ub,
+                                 const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
+cudaError_t launch_decode_mma_bf16(const DecodeParams& p, int head_dim, int block_size, int group, int ub,
+                                  const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
 
 namespace {
 
@@ -104,14 +108,21 @@ DecodeWorkspaceLayout decode_workspace_layout(int num_seqs, int num_heads, int m
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int block_size, int group,
-                          int grid_items_upper_bound, cudaStream_t stream) {
+                          int grid_items_upper_bound, DecodeVariant variant, const CUtensorMap* tmap_k,
+                          const CUtensorMap* tmap_v, cudaStream_t stream) {
+    const int ub = grid_items_upper_bound;
+    const bool mma = variant == kDecodeMma && dtype != PA_F32 && tmap_k && tmap_v;
     decode_plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     switch (dtype) {
-        case PA_F32: return launch_decode_f32(p, head_dim, block_size, group, grid_items_upper_bound, stream);
-        case PA_F16: return launch_decode_f16(p, head_dim, block_size, group, grid_items_upper_bound, stream);
-        case PA_BF16: return launch_decode_bf16(p, head_dim, block_size, group, grid_items_upper_bound, stream);
+        case PA_F32: return launch_decode_f32(p, head_dim, block_size, group, ub, stream);
+        case PA_F16:
+            return mma ? launch_decode_mma_f16(p, head_dim, block_size, group, ub, *tmap_k, *tmap_v, stream)
+                       : launch_decode_simt_f16(p, head_dim, block_size, group, ub, stream);
+        case PA_BF16:
+            return mma ? launch_decode_mma_bf16(p, head_dim, block_size, group, ub, *tmap_k, *tmap_v, stream)
+                       : launch_decode_simt_bf16(p, head_dim, block_size, group, ub, stream);
         default: return cudaErrorNotSupported;
     }
 }

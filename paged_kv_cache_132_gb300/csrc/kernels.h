@@ -2,6 +2,7 @@
 // kernel translation units.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -66,9 +67,16 @@ DecodeWorkspaceLayout decode_workspace_layout(int num_seqs, int num_heads, int m
 // size; partition sizes are multiples of it.
 int decode_stage_tokens(int head_dim, int elem_bytes);
 
-// Launch the planning kernel and the decode kernel on `stream`.
+// Which decode consumer runs: the tensor-core one (16-bit pools, needs the
+// two tensor maps) or the CUDA-core one (every dtype).
+enum DecodeVariant { kDecodeMma = 0, kDecodeSimt = 1 };
+
+// Launch the planning kernel and the decode kernel on `stream`.  tmap_k /
+// tmap_v describe the K and V pools as 2-D tensors [rows = NB*Hkv*B][d] for
+// the tensor-core variant (ignored by the CUDA-core one).
 // Returns cudaErrorNotSupported when no kernel exists for the shape.
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int block_size, int group,
-                          int grid_items_upper_bound, cudaStream_t stream);
+                          int grid_items_upper_bound, DecodeVariant variant, const CUtensorMap* tmap_k,
+                          const CUtensorMap* tmap_v, cudaStream_t stream);
 
 }  // namespace pa

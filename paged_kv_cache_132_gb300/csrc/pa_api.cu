@@ -4,9 +4,12 @@
 // Every argument error is caught here, before anything reaches the GPU; the
 // kernels only report what depends on device data (ids, slots, lengths) or on
 // time (a bounded wait that ran out), through the error word.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstring>
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
@@ -97,6 +100,47 @@ int max_parts_for(int max_context_len, int partition) {
 }
 
 bool partition_ok(int32_t partition_size) { return partition_size == 0 || (partition_size > 0 && partition_size % 64 == 0); }
+
+// cuTensorMapEncodeTiled, fetched through the runtime so that the library
+// does not link against the driver library directly.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// The pool [NB][Hkv][B][d] as a 2-D tensor of NB*Hkv*B rows of d 16-bit
+// elements; a box is 64 elements (128 bytes, the swizzle span) x B rows.
+bool encode_pool_map(CUtensorMap* map, const void* base, int dtype, const pa::PoolShape& shape) {
+    const int64_t rows = shape.num_blocks * shape.num_kv_heads * shape.block_size;
+    if (rows <= 0 || rows >= (1LL << 31) || shape.head_dim % 64 != 0) return false;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)shape.head_dim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)shape.head_dim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)shape.block_size};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    std::memset(map, 0, sizeof(*map));
+    const CUresult r = encode(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                              2, const_cast<void*>(base), dims, strides, box, elem_strides,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Decode consumer: PA_DECODE_KERNEL=simt selects the CUDA-core kernels for
+// 16-bit pools too (the tensor-core ones are the default there).
+pa::DecodeVariant requested_variant() {
+    const char* v = std::getenv("PA_DECODE_KERNEL");
+    return (v && std::strcmp(v, "simt") == 0) ? pa::kDecodeSimt : pa::kDecodeMma;
+}
 
 int status_of(cudaError_t e) {
     if (e == cudaSuccess) return PA_OK;
@@ -221,8 +265,14 @@ int pa_decode(void* out, int32_t out_dtype, const void* query, const void* k_cac
     p.part_o = reinterpret_cast<float*>(ws + lay.part_o);
     p.err = err;
     p.wait_limit_ns = wait_limit_ns();
+
+    pa::DecodeVariant variant = requested_variant();
+    CUtensorMap tmap_k, tmap_v;
+    if (cache->dtype == PA_F32 || !encode_pool_map(&tmap_k, k_cache, cache->dtype, shape) ||
+        !encode_pool_map(&tmap_v, v_cache, cache->dtype, shape))
+        variant = pa::kDecodeSimt;
     return status_of(pa::launch_decode(p, cache->dtype, shape.head_dim, shape.block_size, group, (int)items_ub,
-                                       static_cast<cudaStream_t>(stream)));
+                                       variant, &tmap_k, &tmap_v, static_cast<cudaStream_t>(stream)));
 }
 
 int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers, const int64_t* src_dst_pairs,

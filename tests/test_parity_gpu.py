@@ -20,6 +20,17 @@ def _library():
     native.load()  # raises if the library was not built: no fallback
 
 
+@pytest.fixture(params=["mma", "simt"])
+def kernel(request, monkeypatch):
+    """Run the test with the tensor-core decode kernel (the default for 16-bit
+    pools) and again with the CUDA-core one."""
+    if request.param == "simt":
+        monkeypatch.setenv("PA_DECODE_KERNEL", "simt")
+    else:
+        monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
+    return request.param
+
+
 def _check_step(w, **kw):
     k, v, out, status, code = gpu_step(w, **kw)
     assert status == 0 and code == 0, f"device error {status} / {code:#x}"
@@ -33,7 +44,7 @@ def _check_step(w, **kw):
 
 
 @pytest.mark.parametrize("name", ["tiny", "opt13b", "llama8b", "parallel_sampling"])
-def test_workload_step(name):
+def test_workload_step(name, kernel):
     w = workloads.make(name, device="cuda")
     out, ref, _, _ = _check_step(w)
     if name == "tiny":
@@ -42,12 +53,12 @@ def test_workload_step(name):
 
 
 @pytest.mark.parametrize("block_size", [8, 16, 32])
-def test_long_context_step(block_size):
+def test_long_context_step(block_size, kernel):
     w = workloads.make("long_context", device="cuda", block_size=block_size)
     _check_step(w)
 
 
-def test_long_context_independent_of_block_size():
+def test_long_context_independent_of_block_size(kernel):
     outs = []
     for bs in (8, 16, 32):
         w = workloads.make("long_context", device="cuda", block_size=bs, num_seqs=2)
@@ -58,7 +69,7 @@ def test_long_context_independent_of_block_size():
     assert torch.max(torch.abs(outs[0] - outs[2])) < 1e-5
 
 
-def test_output_in_query_dtype():
+def test_output_in_query_dtype(kernel):
     w = workloads.make("llama8b", device="cuda", num_seqs=64)
     k, v, out, status, _ = gpu_step(w, out_dtype=torch.bfloat16)
     assert status == 0 and out.dtype == torch.bfloat16
@@ -67,7 +78,7 @@ def test_output_in_query_dtype():
 
 
 @pytest.mark.parametrize("partition", [64, 128, 192, 512, 4096])
-def test_forced_partitions(partition):
+def test_forced_partitions(partition, kernel):
     w = workloads.make("llama8b", device="cuda", num_seqs=48)
     _check_step(w, partition_size=partition)
 
@@ -79,7 +90,7 @@ LENGTHS = [0, 1, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 129, 200, 513
 @pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("block_size", [8, 16, 32])
 @pytest.mark.parametrize("group", [1, 2, 4, 8])
-def test_shape_matrix(dtype, head_dim, block_size, group):
+def test_shape_matrix(dtype, head_dim, block_size, group, kernel):
     w = workloads.custom(LENGTHS, num_heads=2 * group, num_kv_heads=2, head_dim=head_dim, block_size=block_size,
                          dtype=dtype, num_blocks=None, device="cuda",
                          seed=7000 + head_dim + block_size + 10 * group)
@@ -87,7 +98,7 @@ def test_shape_matrix(dtype, head_dim, block_size, group):
         _check_step(w, partition_size=partition)
 
 
-def test_block_relabelling_invariance():
+def test_block_relabelling_invariance(kernel):
     w = workloads.make("llama8b", device="cuda", num_seqs=32)
     _, _, base, status, _ = gpu_step(w)
     assert status == 0
@@ -109,7 +120,7 @@ def test_block_relabelling_invariance():
     assert torch.max(torch.abs(base - again)) <= 1e-6
 
 
-def test_shared_prefix_equals_private_copies():
+def test_shared_prefix_equals_private_copies(kernel):
     w = workloads.make("parallel_sampling", device="cuda", num_seqs=32)
     _, _, shared, status, _ = gpu_step(w)
     assert status == 0
@@ -211,7 +222,7 @@ def test_workspace_too_small_is_rejected():
     assert e.value.status == -3
 
 
-def test_repeated_calls_reuse_workspace():
+def test_repeated_calls_reuse_workspace(kernel):
     w = workloads.make("llama8b", device="cuda", num_seqs=64)
     k, v, first, status, _ = gpu_step(w)
     ws = torch.empty(api.decode_workspace_size(w.num_seqs, w.num_heads, w.max_context_len, 64, w.head_dim),
