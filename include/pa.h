@@ -92,8 +92,9 @@ int pa_reshape_and_cache(const void *key, const void *value, void *k_cache, void
  * Bytes of device workspace pa_decode needs for a batch of at most num_seqs
  * sequences, num_heads query heads and contexts of at most max_context_len
  * tokens, at the given partition_size (0 = automatic choice).  The workspace
- * holds the work list, the per-(sequence, KV head) merge counters and the
- * per-partition partial results (running max, sum, normalised output, fp32).
+ * holds the work list, the list of sequences split into several partitions,
+ * and the per-partition partial results (running max, sum, normalised
+ * output, fp32) that the cross-partition merge reads.
  * pa_decode resets what it needs at the start of every call, so the workspace
  * needs no initialisation; two calls in flight at once must not share one.
  * Returns 0 for invalid arguments.

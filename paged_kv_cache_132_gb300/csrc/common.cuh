@@ -17,23 +17,6 @@ namespace pa {
 // ---------------------------------------------------------------------------
 // element types
 // ---------------------------------------------------------------------------
-template <typename T> struct Elem;
-template <> struct Elem<float> {
-    static constexpr int kDtype = PA_F32;
-    __device__ static inline float to_float(float x) { return x; }
-    __device__ static inline float from_float(float x) { return x; }
-};
-template <> struct Elem<__half> {
-    static constexpr int kDtype = PA_F16;
-    __device__ static inline float to_float(__half x) { return __half2float(x); }
-    __device__ static inline __half from_float(float x) { return __float2half_rn(x); }
-};
-template <> struct Elem<__nv_bfloat16> {
-    static constexpr int kDtype = PA_BF16;
-    __device__ static inline float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
-    __device__ static inline __nv_bfloat16 from_float(float x) { return __float2bfloat16_rn(x); }
-};
-
 // Unpack one 16-byte chunk (4 x f32, or 8 x 16-bit) to fp32.
 __device__ inline void unpack16(const uint4& w, float* out, float) {
     out[0] = __uint_as_float(w.x);
@@ -136,10 +119,11 @@ __device__ inline void bulk_copy_g2s(void* smem_dst, const void* gmem_src, uint3
         : "memory");
 }
 
-// Named barrier over the first `threads` threads (warp multiples) of the CTA.
-__device__ inline void named_barrier(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
+// Programmatic dependent launch: let the next kernel in the stream start
+// launching, and (in that kernel) wait until the previous one has completed
+// and its memory is visible.  Without the launch attribute both are no-ops.
+__device__ inline void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ inline void pdl_wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ inline void set_error(int* err, int bits) {
     if (err) atomicOr(err, bits);

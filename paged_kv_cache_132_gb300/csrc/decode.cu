@@ -1,12 +1,19 @@
-// decode.cu -- the planning kernel of a decode call, the workspace layout and
-// the dispatch to the element-type translation units.
+// decode.cu -- the planning and reduce kernels of a decode call, the
+// workspace layout, and the launch sequence plan -> decode -> reduce.
 //
-// The planning kernel turns the context lengths into the work list of
+// Planning kernel: turns the context lengths into the work list of
 // (sequence, partition) pairs -- a sequence of n tokens has ceil(n / P)
-// partitions of P tokens, at least one -- resets the work counter and the
-// per-(sequence, KV head) merge counters, and records the item count.  It
-// runs first in the stream, so the decode kernel finds a ready list and a
-// clean workspace on every call.
+// partitions of P tokens, at least one -- lists the sequences that have more
+// than one partition, and resets the work counter.  It runs first in the
+// stream, so every call finds a ready list and a clean workspace.
+//
+// Reduce kernel: the cross-partition merge of split-KV ("combine the partial
+// results", "PagedAttention paper review", "How does this work?"): for each
+// (sequence, query head) with partitions p = 0..P-1 holding the running max
+// m_p, sum l_p and normalised output o_p,
+//     M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  o = sum_p (l_p 2^(m_p - M) / L) o_p.
+// One warp per (sequence, query head); lanes hold 4 consecutive dims, so a
+// warp-wide load of one partition's output is one contiguous 512-byte row.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -26,15 +33,43 @@ cudaError_t launch_decode_mma_bf16(const DecodeParams& p, int head_dim, int bloc
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kReduceThreads = 256;
+
+// Inclusive scan of x over the CTA (kPlanThreads threads); `scratch` holds
+// one int per warp.
+__device__ int block_inclusive_scan(int x, int* scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = scratch[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, off);
+            if (lane >= off) t += y;
+        }
+        scratch[lane] = t;
+    }
+    __syncthreads();
+    const int r = x + (warp > 0 ? scratch[warp - 1] : 0);
+    __syncthreads();
+    return r;
+}
 
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const __grid_constant__ DecodeParams p) {
-    __shared__ int warp_total[32];
-    __shared__ int carry;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t units = (int64_t)p.num_seqs * p.num_kv_heads;
-    for (int64_t i = tid; i < units; i += kPlanThreads) p.counters[i] = 0;
+    __shared__ int scratch[32];
+    __shared__ int carry[2];
+    // The decode kernel may launch now; it waits for this grid to complete
+    // before it reads the work list.
+    pdl_launch_dependents();
+    const int tid = threadIdx.x;
     if (tid == 0) {
-        carry = 0;
+        carry[0] = carry[1] = 0;
         *p.next_item = 0;
     }
     __syncthreads();
@@ -49,33 +84,119 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const __grid_
             }
             np = ctx == 0 ? 1 : (ctx + p.partition_size - 1) / p.partition_size;
         }
-        // Inclusive scan of np over the CTA.
-        int x = np;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, off);
-            if (lane >= off) x += y;
-        }
-        if (lane == 31) warp_total[warp] = x;
-        __syncthreads();
-        if (warp == 0) {
-            int t = warp_total[lane];
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, t, off);
-                if (lane >= off) t += y;
-            }
-            warp_total[lane] = t;
-        }
-        __syncthreads();
-        const int inclusive = x + (warp > 0 ? warp_total[warp - 1] : 0);
-        const int first = carry + inclusive - np;
+        const int multi = np > 1 ? 1 : 0;
+        const int items_incl = block_inclusive_scan(np, scratch);
+        const int multi_incl = block_inclusive_scan(multi, scratch);
+        const int first = carry[0] + items_incl - np;
         for (int k = 0; k < np; ++k) p.items[first + k] = make_int2(s, k);
+        if (multi) p.multi_seqs[carry[1] + multi_incl - 1] = s;
         __syncthreads();
-        if (tid == kPlanThreads - 1) carry += inclusive;
+        if (tid == kPlanThreads - 1) {
+            carry[0] += items_incl;
+            carry[1] += multi_incl;
+        }
         __syncthreads();
     }
-    if (tid == 0) *p.num_items = carry * p.num_kv_heads;
+    if (tid == 0) {
+        *p.num_items = carry[0] * p.num_kv_heads;
+        *p.num_multi = carry[1];
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kReduceThreads) decode_reduce_kernel(const __grid_constant__ DecodeParams p,
+                                                                        int group) {
+    constexpr int VPL = D / 32;  // dims per lane (2 or 4)
+    pdl_wait_prerequisites();    // the decode kernel wrote the partials
+    const float NEG_INF = __int_as_float(0xff800000);
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (kReduceThreads / 32);
+    const int per_seq = p.num_kv_heads * group;
+    const int64_t total = (int64_t)*p.num_multi * per_seq;
+    for (int64_t w = blockIdx.x * (kReduceThreads / 32) + (threadIdx.x >> 5); w < total; w += warps) {
+        const int s = p.multi_seqs[w / per_seq];
+        const int hq = (int)(w % per_seq);  // query head s*H + hq
+        const int h = hq / group, g = hq - h * group;
+        int ctx = p.context_lens[s];
+        ctx = ctx < 0 ? 0 : (ctx > p.ctx_cap ? p.ctx_cap : ctx);
+        const int nparts = (ctx + p.partition_size - 1) / p.partition_size;
+        const int64_t base = ((int64_t)s * p.num_kv_heads + h) * p.max_parts * group + g;
+        // Max and sum over the partitions, lanes striding over them.
+        float M = NEG_INF;
+        for (int q = lane; q < nparts; q += 32) M = fmaxf(M, __ldcg(p.part_ml + 2 * (base + (int64_t)q * group)));
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float L = 0.f;
+        for (int q = lane; q < nparts; q += 32) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + 2 * (base + (int64_t)q * group)));
+            L += ml.y * exp2_approx(ml.x - M);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        const float invL = 1.f / L;
+        // Weighted sum of the partial outputs; lane q%32 holds partition q's weight.
+        float acc[VPL];
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) acc[v] = 0.f;
+        for (int q0 = 0; q0 < nparts; q0 += 32) {
+            float wq = 0.f;
+            if (q0 + lane < nparts) {
+                const float2 ml =
+                    __ldcg(reinterpret_cast<const float2*>(p.part_ml + 2 * (base + (int64_t)(q0 + lane) * group)));
+                wq = ml.y * exp2_approx(ml.x - M) * invL;
+            }
+            const int n = min(32, nparts - q0);
+#pragma unroll 8
+            for (int k = 0; k < n; ++k) {
+                const float wk = __shfl_sync(0xffffffffu, wq, k);
+                const float* src = p.part_o + (base + (int64_t)(q0 + k) * group) * D + lane * VPL;
+                if constexpr (VPL == 4) {
+                    const float4 o = __ldcg(reinterpret_cast<const float4*>(src));
+                    acc[0] = fmaf(wk, o.x, acc[0]);
+                    acc[1] = fmaf(wk, o.y, acc[1]);
+                    acc[2] = fmaf(wk, o.z, acc[2]);
+                    acc[3] = fmaf(wk, o.w, acc[3]);
+                } else {
+                    const float2 o = __ldcg(reinterpret_cast<const float2*>(src));
+                    acc[0] = fmaf(wk, o.x, acc[0]);
+                    acc[1] = fmaf(wk, o.y, acc[1]);
+                }
+            }
+        }
+        const int64_t oi = ((int64_t)s * p.num_heads + (int64_t)h * group + g) * D + lane * VPL;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            if (p.out_dtype == PA_F32)
+                static_cast<float*>(p.out)[oi + v] = acc[v];
+            else if (p.out_dtype == PA_F16)
+                static_cast<__half*>(p.out)[oi + v] = __float2half_rn(acc[v]);
+            else
+                static_cast<__nv_bfloat16*>(p.out)[oi + v] = __float2bfloat16_rn(acc[v]);
+        }
+    }
+}
+
+cudaError_t launch_reduce(const DecodeParams& p, int head_dim, int group, cudaStream_t stream) {
+    int dev = 0, sms = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    // Upper bound of the warps needed; the kernel strides over the real count.
+    const int64_t work = (int64_t)p.num_seqs * p.num_heads;
+    int64_t ctas = (work + kReduceThreads / 32 - 1) / (kReduceThreads / 32);
+    if (ctas > 4LL * sms) ctas = 4LL * sms;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(ctas > 0 ? ctas : 1));
+    cfg.blockDim = dim3(kReduceThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (head_dim == 64) return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<64>, p, group);
+    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<128>, p, group);
+    return cudaErrorNotSupported;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -91,14 +212,14 @@ int decode_stage_tokens(int head_dim, int elem_bytes) {
 DecodeWorkspaceLayout decode_workspace_layout(int num_seqs, int num_heads, int max_parts, int head_dim) {
     DecodeWorkspaceLayout w{};
     const size_t s = (size_t)num_seqs, h = (size_t)num_heads, mp = (size_t)max_parts;
-    size_t off = 0;
-    w.next_item = off;
-    w.num_items = off + 4;
-    off = 256;
+    w.next_item = 0;
+    w.num_items = 4;
+    w.num_multi = 8;
+    size_t off = 256;
     w.items = off;
     off = align_up(off + s * mp * sizeof(int2), 256);
-    w.counters = off;
-    off = align_up(off + s * h * sizeof(int), 256);
+    w.multi_seqs = off;
+    off = align_up(off + s * sizeof(int), 256);
     w.part_ml = off;
     off = align_up(off + s * h * mp * 2 * sizeof(float), 256);
     w.part_o = off;
@@ -116,15 +237,21 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int bl
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     switch (dtype) {
-        case PA_F32: return launch_decode_f32(p, head_dim, block_size, group, ub, stream);
+        case PA_F32: e = launch_decode_f32(p, head_dim, block_size, group, ub, stream); break;
         case PA_F16:
-            return mma ? launch_decode_mma_f16(p, head_dim, block_size, group, ub, *tmap_k, *tmap_v, stream)
-                       : launch_decode_simt_f16(p, head_dim, block_size, group, ub, stream);
+            e = mma ? launch_decode_mma_f16(p, head_dim, block_size, group, ub, *tmap_k, *tmap_v, stream)
+                    : launch_decode_simt_f16(p, head_dim, block_size, group, ub, stream);
+            break;
         case PA_BF16:
-            return mma ? launch_decode_mma_bf16(p, head_dim, block_size, group, ub, *tmap_k, *tmap_v, stream)
-                       : launch_decode_simt_bf16(p, head_dim, block_size, group, ub, stream);
+            e = mma ? launch_decode_mma_bf16(p, head_dim, block_size, group, ub, *tmap_k, *tmap_v, stream)
+                    : launch_decode_simt_bf16(p, head_dim, block_size, group, ub, stream);
+            break;
         default: return cudaErrorNotSupported;
     }
+    if (e != cudaSuccess) return e;
+    // With a single partition per sequence every output is already final.
+    if (p.max_parts > 1) e = launch_reduce(p, head_dim, group, stream);
+    return e;
 }
 
 }  // namespace pa

@@ -8,10 +8,9 @@
 // and the per-block results are combined exactly ("PagedAttention paper
 // review", "How does this work?") by the running-max / running-sum softmax.
 // A context longer than the partition size is split into partitions that
-// different CTAs compute; the CTA that finishes the last partition of a
-// (sequence, KV head) merges them with
-//     M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  o = sum_p (l_p 2^(m_p - M) / L) o_p
-// (scores are kept in base-2 units: scale * log2 e is folded in).
+// different CTAs compute; each stores its (max, sum, normalised output) and
+// the reduce kernel (decode.cu) merges them.  Scores are kept in base-2 units
+// (scale * log2 e is folded in).
 //
 // CTA structure (persistent, one or two CTAs per SM):
 //   producer warp: takes (sequence, partition, KV head) items from a device
@@ -22,7 +21,10 @@
 //     "Efficient Memory Management ... Review", §3-2).
 //   consumer warps: each takes a quarter of a stage's tokens and keeps its own
 //     running max / sum / output for the G query heads of the KV head (GQA
-//     grouping on the CTA).  At an item's end they merge through shared memory.
+//     grouping on the CTA).  At an item's end they leave their state in a
+//     shared-memory slot and go on with the next item.
+//   merge warp: merges the consumer warps' states of a finished item and
+//     stores the output, or the partition's partial for the reduce kernel.
 // Every wait is bounded by a wall-time limit; a wait that runs out sets
 // PA_DEVERR_TIMEOUT, and the CTA drains its copies and returns.
 #pragma once
@@ -61,7 +63,9 @@ struct DecodeShape {
     static constexpr int E = sizeof(T);
     static constexpr int NCW = kDecodeConsumerWarps;
     static constexpr int NSTAGE = kDecodeStages;
-    static constexpr int THREADS = (NCW + 1) * 32;
+    static constexpr int PRODUCER_WARP = NCW;         // fills the stage ring
+    static constexpr int MERGE_WARP = NCW + 1;        // merges and stores finished items
+    static constexpr int THREADS = (NCW + 2) * 32;
     static constexpr int ROW = D * E;                 // bytes of one token's row
     static constexpr int STAGE_TOK = stage_tokens_for_row(ROW);
     static_assert(STAGE_TOK % BS == 0, "a stage holds whole blocks");
@@ -72,21 +76,21 @@ struct DecodeShape {
     static constexpr int KV_STAGE_BYTES = STAGE_TOK * ROW;
     static constexpr int QBYTES = G * D * E;
     static_assert(QBYTES % 16 == 0, "the q tile is one bulk copy");
+    static_assert(D % 128 == 0 || D == 64, "the merge warp stores 4 consecutive dims per lane");
 
     struct Smem {
         alignas(1024) uint8_t kv[NSTAGE][2][KV_STAGE_BYTES];
         alignas(16) uint8_t q[NSTAGE][QBYTES];
-        float mo[NCW][G][D];   // per-warp output accumulators at the item's end
+        alignas(16) float mo[NCW][G][D];   // per-warp output accumulators of the finished item
         float mm[NCW][G];      // per-warp running max (base-2 units)
         float ml[NCW][G];      // per-warp running sum
-        float fin_m[G];        // merged max / sum over partitions
-        float fin_l[G];
         StageMeta meta[NSTAGE];
+        StageMeta merge_meta;  // the finished item handed to the merge warp
         uint64_t full[NSTAGE];
         uint64_t empty[NSTAGE];
-        uint64_t group_bar;    // consumer-warp barrier
+        uint64_t merge_full;   // consumers -> merge warp: the slot holds an item
+        uint64_t merge_free;   // merge warp -> consumers: the slot may be reused
         int abort_flag;
-        int is_last;
     };
     // 1 KiB of slack to align the dynamic shared memory base to 1024 bytes.
     static constexpr int SMEM_BYTES = sizeof(Smem) + 1024;
@@ -105,12 +109,15 @@ __device__ inline void decode_smem_init(Smem& sm, int stages, int consumer_warps
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], consumer_warps);
         }
-        mbar_init(&sm.group_bar, consumer_warps * 32);
+        mbar_init(&sm.merge_full, consumer_warps);
+        mbar_init(&sm.merge_free, 1);
         sm.abort_flag = 0;
-        sm.is_last = 0;
         fence_mbar_init();
     }
     __syncthreads();
+    // The planning kernel before this one writes the work list; wait for it
+    // (the set-up above overlapped with it).
+    pdl_wait_prerequisites();
 }
 
 // 2-D tiled TMA load of one box into shared memory, completed on `bar`.
@@ -121,23 +128,22 @@ __device__ inline void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x
         : "memory");
 }
 
-// Consumer-group barrier on an mbarrier (count = consumer threads) with a
-// bounded wait, so that a CTA whose wait ran out cannot hang its siblings.
-template <class Smem>
-__device__ inline bool group_sync(Smem& sm, uint32_t& phase, unsigned long long limit) {
-    mbar_arrive(&sm.group_bar);
-    const bool ok = mbar_wait_bounded(&sm.group_bar, phase, limit);
-    phase ^= 1u;
-    return __all_sync(kFullMask, ok);
-}
-
-__device__ inline void store_out(void* out, int dtype, int64_t index, float v) {
-    if (dtype == PA_F32)
-        static_cast<float*>(out)[index] = v;
-    else if (dtype == PA_F16)
-        static_cast<__half*>(out)[index] = __float2half_rn(v);
-    else
-        static_cast<__nv_bfloat16*>(out)[index] = __float2bfloat16_rn(v);
+__device__ inline void store_out4(void* out, int dtype, int64_t index, float4 v) {
+    if (dtype == PA_F32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(out) + index) = v;
+    } else if (dtype == PA_F16) {
+        __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+        uint2 w;
+        memcpy(&w.x, &a, 4);
+        memcpy(&w.y, &b, 4);
+        *reinterpret_cast<uint2*>(static_cast<__half*>(out) + index) = w;
+    } else {
+        __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        uint2 w;
+        memcpy(&w.x, &a, 4);
+        memcpy(&w.y, &b, 4);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + index) = w;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -164,24 +170,29 @@ __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm,
     unsigned total_fills = 0;
     bool aborted = false;
 
+    // Item metadata travels one item ahead: while item k streams, the id of
+    // item k+1, its (sequence, partition) pair and its context length are
+    // already being fetched, so a new item starts without dependent loads.
+    auto item_pair = [&](int it) { return it < num_items ? p.items[it / p.num_kv_heads] : make_int2(0, 0); };
     int item = 0;
     if (lane == 0) item = atomicAdd(p.next_item, 1);
     item = __shfl_sync(kFullMask, item, 0);
+    int2 sp = item_pair(item);
+    int ctx_raw = item < num_items ? __ldg(p.context_lens + sp.x) : 0;
     while (item < num_items) {
         int next = 0;
-        if (lane == 0) next = atomicAdd(p.next_item, 1);  // its latency overlaps this item
-        const int pair = item / p.num_kv_heads;
-        const int h = item - pair * p.num_kv_heads;
-        const int2 sp = p.items[pair];
+        if (lane == 0) next = atomicAdd(p.next_item, 1);
+        const int h = item - (item / p.num_kv_heads) * p.num_kv_heads;
         const int s = sp.x, part = sp.y;
-        int ctx = __ldg(p.context_lens + s);
-        ctx = ctx < 0 ? 0 : (ctx > p.ctx_cap ? p.ctx_cap : ctx);
+        const int ctx = ctx_raw < 0 ? 0 : (ctx_raw > p.ctx_cap ? p.ctx_cap : ctx_raw);
         const int nparts = ctx == 0 ? 1 : (ctx + part_size - 1) / part_size;
         const int tb = part * part_size;
         const int te = min(tb + part_size, ctx);
         const int ntok = te > tb ? te - tb : 0;
         const int nst = ntok == 0 ? 1 : (ntok + Shape::STAGE_TOK - 1) / Shape::STAGE_TOK;
         const int32_t* trow = p.block_tables + (int64_t)s * p.max_blocks;
+        int2 sp_next = make_int2(0, 0);
+        int ctx_next = 0;
 
         for (int c = 0; c < nst; ++c) {
             const int t0 = tb + c * Shape::STAGE_TOK;
@@ -242,9 +253,17 @@ __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm,
                 st = 0;
                 ph ^= 1u;
             }
+            if (c == 0) {
+                // Start fetching the next item's metadata.
+                next = __shfl_sync(kFullMask, next, 0);
+                sp_next = item_pair(next);
+                ctx_next = next < num_items ? __ldg(p.context_lens + sp_next.x) : 0;
+            }
         }
         if (aborted) break;
-        item = __shfl_sync(kFullMask, next, 0);
+        item = next;
+        sp = sp_next;
+        ctx_raw = ctx_next;
     }
 
     if (!aborted) {
@@ -266,6 +285,8 @@ __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm,
         set_error(p.err, PA_DEVERR_TIMEOUT);
         atomicExch(&sm.abort_flag, 1);
     }
+    // This CTA takes no more work: the reduce kernel may start launching.
+    pdl_launch_dependents();
     // Drain: every copy this warp issued must land before the CTA exits.
     if (lane == 0) {
         for (int j = 0; j < Shape::NSTAGE; ++j) {
@@ -280,100 +301,77 @@ __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm,
 }
 
 // ---------------------------------------------------------------------------
-// end of an item: merge the consumer warps' (max, sum, output) held in
-// sm.mm / sm.ml / sm.mo, then write the output (one partition) or a partial
-// and, in the CTA that completes a (sequence, KV head), merge all partials.
-// Called by all consumer threads; returns false if a bounded wait ran out.
+// end of an item
+//   consumers: wait until the merge slot is free, store their per-warp
+//     (max, sum, output) in it, and go on with the next item;
+//   merge warp: merges the consumer warps' states and stores the output (one
+//     partition) or the partition's partial (max, sum, normalised output) for
+//     the reduce kernel.
 // ---------------------------------------------------------------------------
+template <class Smem>
+__device__ inline bool acquire_merge_slot(Smem& sm, uint32_t fph, unsigned long long limit) {
+    const bool ok = mbar_wait_bounded(&sm.merge_free, fph ^ 1u, limit);
+    return __all_sync(kFullMask, ok);
+}
+
+// Called by every consumer warp after it wrote its part of the slot.
+template <class Smem>
+__device__ inline void release_to_merger(Smem& sm, const StageMeta& mt, int warp, int lane) {
+    if (warp == 0 && lane == 0) sm.merge_meta = mt;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.merge_full);
+}
+
 template <class Shape, int D, int G>
-__device__ bool finish_item(const DecodeParams& p, typename Shape::Smem& sm, const StageMeta& mt, int warp, int lane,
-                            uint32_t& gph) {
+__device__ void merge_worker(const DecodeParams& p, typename Shape::Smem& sm, int lane) {
     constexpr int NCW = Shape::NCW;
     const float NEG_INF = __int_as_float(0xff800000);
-    const int ct = warp * 32 + lane;
-    bool gok = group_sync(sm, gph, p.wait_limit_ns);
-    const int s = mt.seq, h = mt.kv_head;
-    const int64_t unit = (int64_t)s * p.num_kv_heads + h;
-    if (gok) {
-        for (int i = ct; i < G * D; i += NCW * 32) {
-            const int g = i / D, dd = i - (i / D) * D;
+    uint32_t mph = 0;
+    while (true) {
+        const bool ok = mbar_wait_bounded(&sm.merge_full, mph, p.wait_limit_ns);
+        if (!__all_sync(kFullMask, ok)) {
+            if (lane == 0) {
+                set_error(p.err, PA_DEVERR_TIMEOUT);
+                atomicExch(&sm.abort_flag, 1);
+            }
+            return;
+        }
+        mph ^= 1u;
+        const StageMeta mt = sm.merge_meta;
+        if (mt.item < 0) return;
+        const int s = mt.seq, h = mt.kv_head;
+        const int64_t unit = (int64_t)s * p.num_kv_heads + h;
+        for (int i = lane; i < G * D / 4; i += 32) {
+            const int g = (4 * i) / D, dd = 4 * i - g * D;
             float M = NEG_INF;
 #pragma unroll
             for (int w = 0; w < NCW; ++w) M = fmaxf(M, sm.mm[w][g]);
-            float L = 0.f, O = 0.f;
+            float L = 0.f;
+            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int w = 0; w < NCW; ++w) {
                 const float mw = sm.mm[w][g];
                 const float f = mw == NEG_INF ? 0.f : exp2_approx(mw - M);
+                const float4 v = *reinterpret_cast<const float4*>(&sm.mo[w][g][dd]);
                 L = fmaf(f, sm.ml[w][g], L);
-                O = fmaf(f, sm.mo[w][g][dd], O);
+                O.x = fmaf(f, v.x, O.x);
+                O.y = fmaf(f, v.y, O.y);
+                O.z = fmaf(f, v.z, O.z);
+                O.w = fmaf(f, v.w, O.w);
             }
-            const float o = L > 0.f ? O / L : 0.f;
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            const float4 o = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
             if (mt.nparts == 1) {
-                store_out(p.out, p.out_dtype, ((int64_t)s * p.num_heads + (int64_t)h * G + g) * D + dd, o);
+                store_out4(p.out, p.out_dtype, ((int64_t)s * p.num_heads + (int64_t)h * G + g) * D + dd, o);
             } else {
                 const int64_t pi = (unit * p.max_parts + mt.part) * G + g;
-                p.part_o[pi * D + dd] = o;
-                if (dd == 0) {
-                    p.part_ml[2 * pi] = M;
-                    p.part_ml[2 * pi + 1] = L;
-                }
+                *reinterpret_cast<float4*>(p.part_o + pi * D + dd) = o;
+                if (dd == 0) *reinterpret_cast<float2*>(p.part_ml + 2 * pi) = make_float2(M, L);
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.merge_free);
     }
-    if (gok && mt.nparts > 1) {
-        __threadfence();
-        gok = group_sync(sm, gph, p.wait_limit_ns);
-        if (gok && ct == 0) {
-            const int done = atomicAdd(p.counters + unit, 1);
-            sm.is_last = done == mt.nparts - 1;
-        }
-        if (gok) gok = group_sync(sm, gph, p.wait_limit_ns);
-        if (gok && sm.is_last) {
-            __threadfence();
-            // Per-head max and sum over the partitions, one warp per head.
-            for (int g = warp; g < G; g += NCW) {
-                const int64_t base = unit * p.max_parts * G + g;
-                float M = NEG_INF;
-                for (int q = lane; q < mt.nparts; q += 32)
-                    M = fmaxf(M, __ldcg(p.part_ml + 2 * (base + (int64_t)q * G)));
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, off));
-                float L = 0.f;
-                for (int q = lane; q < mt.nparts; q += 32) {
-                    const int64_t pi = base + (int64_t)q * G;
-                    L += __ldcg(p.part_ml + 2 * pi + 1) * exp2_approx(__ldcg(p.part_ml + 2 * pi) - M);
-                }
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(kFullMask, L, off);
-                if (lane == 0) {
-                    sm.fin_m[g] = M;
-                    sm.fin_l[g] = L;
-                }
-            }
-            gok = group_sync(sm, gph, p.wait_limit_ns);
-            if (gok) {
-                for (int i = ct; i < G * D; i += NCW * 32) {
-                    const int g = i / D, dd = i - (i / D) * D;
-                    const int64_t base = unit * p.max_parts * G + g;
-                    const float M = sm.fin_m[g];
-                    const float invL = 1.f / sm.fin_l[g];
-                    float O = 0.f;
-#pragma unroll 4
-                    for (int q = 0; q < mt.nparts; ++q) {
-                        const int64_t pi = base + (int64_t)q * G;
-                        const float wgt = __ldcg(p.part_ml + 2 * pi + 1) * exp2_approx(__ldcg(p.part_ml + 2 * pi) - M);
-                        O = fmaf(wgt, __ldcg(p.part_o + pi * D + dd), O);
-                    }
-                    store_out(p.out, p.out_dtype, ((int64_t)s * p.num_heads + (int64_t)h * G + g) * D + dd, O * invL);
-                }
-                if (ct == 0) p.counters[unit] = 0;
-            }
-        }
-    }
-    // The merge buffers are free again only when every warp is done reading.
-    if (gok) gok = group_sync(sm, gph, p.wait_limit_ns);
-    return gok;
 }
 
 __device__ inline void consumer_abort(const DecodeParams& p, int* abort_flag, int lane) {
@@ -397,8 +395,18 @@ cudaError_t launch_persistent(Kernel kernel, int items_upper_bound, cudaStream_t
     if (occ < 1) return cudaErrorInvalidConfiguration;
     int grid = sms * occ;
     if (items_upper_bound < grid) grid = items_upper_bound > 0 ? items_upper_bound : 1;
-    kernel<<<grid, Shape::THREADS, smem, stream>>>(args...);
-    return cudaGetLastError();
+    // Launched as a programmatic dependent of the planning kernel.
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(Shape::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace pa

@@ -102,7 +102,7 @@ __device__ void mma_consumer(const DecodeParams& p, typename DecodeShape<T, D, B
     for (int k = 0; k < KSTEPS; ++k) qa[k][0] = qa[k][1] = 0u;
 
     int st = 0;
-    uint32_t ph = 0, gph = 0;
+    uint32_t ph = 0, fph = 0;
     while (true) {
         const bool ok = mbar_wait_bounded(&sm.full[st], ph, p.wait_limit_ns);
         if (!__all_sync(kFullMask, ok)) {
@@ -110,7 +110,14 @@ __device__ void mma_consumer(const DecodeParams& p, typename DecodeShape<T, D, B
             break;
         }
         const StageMeta mt = sm.meta[st];
-        if (mt.item < 0) break;
+        if (mt.item < 0) {
+            // No more work: tell the merge warp to stop.
+            if (acquire_merge_slot(sm, fph, p.wait_limit_ns)) {
+                StageMeta end = mt;
+                release_to_merger(sm, end, warp, lane);
+            }
+            break;
+        }
 
         if (mt.first) {
             const T* qs = reinterpret_cast<const T*>(sm.q[st]);
@@ -130,10 +137,14 @@ __device__ void mma_consumer(const DecodeParams& p, typename DecodeShape<T, D, B
         if (tok0 < mt.te) {
             const uint32_t kst = smem_addr(sm.kv[st][0]);
             const uint32_t vst = smem_addr(sm.kv[st][1]);
-            // ---- S = Q K^T over two n8 tiles (tokens row0..+7, row0+8..+15)
-            float sacc[2][4];
+            // ---- S = Q K^T over two n8 tiles (tokens row0..+7, row0+8..+15);
+            // even and odd k steps go to separate accumulators (shorter
+            // dependency chains), summed afterwards.
+            float sacc[2][4], sodd[2][4];
 #pragma unroll
-            for (int t = 0; t < 2; ++t) sacc[t][0] = sacc[t][1] = sacc[t][2] = sacc[t][3] = 0.f;
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[t][e] = sodd[t][e] = 0.f;
 #pragma unroll
             for (int kp = 0; kp < KSTEPS / 2; ++kp) {
 #pragma unroll
@@ -142,8 +153,13 @@ __device__ void mma_consumer(const DecodeParams& p, typename DecodeShape<T, D, B
                     ldmatrix_x4(b0, b1, b2, b3,
                                 swizzled_chunk<S::STAGE_TOK>(kst, row0 + t * 8 + (lane & 7), kp * 4 + (lane >> 3)));
                     Ops::mma(sacc[t], qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, b0, b1);
-                    Ops::mma(sacc[t], qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, b2, b3);
+                    Ops::mma(sodd[t], qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, b2, b3);
                 }
+            }
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                sacc[t][0] += sodd[t][0];
+                sacc[t][1] += sodd[t][1];
             }
             // ---- online softmax on row g (tokens 2j, 2j+1, 8+2j, 8+2j+1)
             float sv[4];
@@ -208,9 +224,14 @@ __device__ void mma_consumer(const DecodeParams& p, typename DecodeShape<T, D, B
         if (lane == 0) mbar_arrive(&sm.empty[st]);
 
         if (mt.last) {
+            // Hand the item's state to the merge warp and move on.
             float lw = l;
             lw += __shfl_xor_sync(kFullMask, lw, 1);
             lw += __shfl_xor_sync(kFullMask, lw, 2);
+            if (!acquire_merge_slot(sm, fph, p.wait_limit_ns)) {
+                consumer_abort(p, &sm.abort_flag, lane);
+                break;
+            }
             if (g < G) {
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
@@ -220,10 +241,8 @@ __device__ void mma_consumer(const DecodeParams& p, typename DecodeShape<T, D, B
                     sm.ml[warp][g] = lw;
                 }
             }
-            if (!finish_item<S, D, G>(p, sm, mt, warp, lane, gph)) {
-                consumer_abort(p, &sm.abort_flag, lane);
-                break;
-            }
+            release_to_merger(sm, mt, warp, lane);
+            fph ^= 1u;
         }
         if (++st == S::NSTAGE) {
             st = 0;
@@ -234,7 +253,7 @@ __device__ void mma_consumer(const DecodeParams& p, typename DecodeShape<T, D, B
 }
 
 template <typename T, int D, int BS, int G>
-__global__ void __launch_bounds__(DecodeShape<T, D, BS, G>::THREADS)
+__global__ void __launch_bounds__(DecodeShape<T, D, BS, G>::THREADS, 2)
 decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v) {
     using S = DecodeShape<T, D, BS, G>;
@@ -242,10 +261,12 @@ decode_mma_kernel(const __grid_constant__ DecodeParams p, const __grid_constant_
     auto& sm = decode_smem<typename S::Smem>(smem_raw);
     decode_smem_init(sm, S::NSTAGE, S::NCW);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (warp == S::NCW)
+    if (warp < S::NCW)
+        mma_consumer<T, D, BS, G>(p, sm, warp, lane);
+    else if (warp == S::PRODUCER_WARP)
         decode_producer<S, BS, G, true>(p, sm, lane, &tmap_k, &tmap_v);
     else
-        mma_consumer<T, D, BS, G>(p, sm, warp, lane);
+        merge_worker<S, D, G>(p, sm, lane);
 }
 
 }  // namespace pa

@@ -46,7 +46,7 @@ __device__ void simt_consumer(const DecodeParams& p, typename DecodeShape<T, D, 
     }
 
     int st = 0;
-    uint32_t ph = 0, gph = 0;
+    uint32_t ph = 0, fph = 0;
     while (true) {
         const bool ok = mbar_wait_bounded(&sm.full[st], ph, p.wait_limit_ns);
         if (!__all_sync(kFullMask, ok)) {
@@ -54,7 +54,14 @@ __device__ void simt_consumer(const DecodeParams& p, typename DecodeShape<T, D, 
             break;
         }
         const StageMeta mt = sm.meta[st];
-        if (mt.item < 0) break;
+        if (mt.item < 0) {
+            // No more work: tell the merge warp to stop.
+            if (acquire_merge_slot(sm, fph, p.wait_limit_ns)) {
+                StageMeta end = mt;
+                release_to_merger(sm, end, warp, lane);
+            }
+            break;
+        }
 
         if (mt.first) {
             const T* qs = reinterpret_cast<const T*>(sm.q[st]);
@@ -142,7 +149,12 @@ __device__ void simt_consumer(const DecodeParams& p, typename DecodeShape<T, D, 
         if (lane == 0) mbar_arrive(&sm.empty[st]);
 
         if (mt.last) {
-            // Sum over the warp's row groups, then hand over to the item merge.
+            // Sum over the warp's row groups, then hand the item's state to
+            // the merge warp and move on.
+            if (!acquire_merge_slot(sm, fph, p.wait_limit_ns)) {
+                consumer_abort(p, &sm.abort_flag, lane);
+                break;
+            }
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 float lw = l[g];
@@ -160,10 +172,8 @@ __device__ void simt_consumer(const DecodeParams& p, typename DecodeShape<T, D, 
                     sm.ml[warp][g] = lw;
                 }
             }
-            if (!finish_item<Base, D, G>(p, sm, mt, warp, lane, gph)) {
-                consumer_abort(p, &sm.abort_flag, lane);
-                break;
-            }
+            release_to_merger(sm, mt, warp, lane);
+            fph ^= 1u;
         }
         if (++st == Base::NSTAGE) {
             st = 0;
@@ -174,17 +184,19 @@ __device__ void simt_consumer(const DecodeParams& p, typename DecodeShape<T, D, 
 }
 
 template <typename T, int D, int BS, int G>
-__global__ void __launch_bounds__(DecodeShape<T, D, BS, G>::THREADS)
+__global__ void __launch_bounds__(DecodeShape<T, D, BS, G>::THREADS, 2)
 decode_simt_kernel(const __grid_constant__ DecodeParams p) {
     using S = DecodeShape<T, D, BS, G>;
     extern __shared__ uint8_t smem_raw[];
     auto& sm = decode_smem<typename S::Smem>(smem_raw);
     decode_smem_init(sm, S::NSTAGE, S::NCW);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (warp == S::NCW)
+    if (warp < S::NCW)
+        simt_consumer<T, D, BS, G>(p, sm, warp, lane);
+    else if (warp == S::PRODUCER_WARP)
         decode_producer<S, BS, G, false>(p, sm, lane, nullptr, nullptr);
     else
-        simt_consumer<T, D, BS, G>(p, sm, warp, lane);
+        merge_worker<S, D, G>(p, sm, lane);
 }
 
 }  // namespace pa

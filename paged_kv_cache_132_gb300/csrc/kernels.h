@@ -50,7 +50,8 @@ struct DecodeParams {
     int* next_item;            // dynamic work counter
     int* num_items;            // (sequence, partition) pairs x num_kv_heads
     int2* items;               // (sequence, partition) pairs
-    int* counters;             // [num_seqs * num_kv_heads] partitions finished
+    int* num_multi;            // sequences with more than one partition
+    int* multi_seqs;           // [num_seqs] their indices
     float* part_ml;            // [num_seqs * num_kv_heads * max_parts * G][2] (max, sum)
     float* part_o;             // [num_seqs * num_kv_heads * max_parts * G][head_dim]
     int* err;                  // device error word
@@ -58,7 +59,7 @@ struct DecodeParams {
 };
 
 struct DecodeWorkspaceLayout {
-    size_t next_item, num_items, items, counters, part_ml, part_o, total;
+    size_t next_item, num_items, num_multi, items, multi_seqs, part_ml, part_o, total;
 };
 
 DecodeWorkspaceLayout decode_workspace_layout(int num_seqs, int num_heads, int max_parts, int head_dim);
