@@ -132,6 +132,37 @@ int pa_decode(void *out, int32_t out_dtype, const void *query,
               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Size of the device array pa_decode_noalloc uses as its workspace: 32 MiB,
+ * reserved on every GPU that loads the library, until the process exits.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * pa_decode without a caller-provided workspace, for callers that cannot
+ * allocate device memory: an engine that reserved all of its GPU memory up
+ * front and forbids later allocations, code that must not block on an
+ * allocator or a device-wide synchronisation, or a plugin whose host owns all
+ * device memory.  The paper has no counterpart of this call; it exists for
+ * those callers only.  The arguments mean what they mean for pa_decode; the
+ * workspace is a fixed array of PA_NOALLOC_SCRATCH_BYTES inside the library.
+ *   - Nothing is allocated: no cudaMalloc, no cudaFree, no allocator call.
+ *   - A batch whose workspace (pa_decode_workspace_size) exceeds the array
+ *     returns PA_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make it before any stream
+ *     capture.
+ *   - All calls share the array, which keeps the last call's contents (each
+ *     call resets what it needs).  Calls whose work overlaps on the GPU --
+ *     other streams or host threads -- race on it; serialise them.
+ */
+int pa_decode_noalloc(void *out, int32_t out_dtype, const void *query,
+                      const void *k_cache, const void *v_cache, const pa_cache_desc *cache,
+                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                      const int32_t *context_lens, int32_t num_seqs, int32_t max_context_len,
+                      int32_t num_heads, int32_t num_kv_heads, float scale, int32_t partition_size,
+                      void *stream);
+
+/*
  * Copy-on-write block copy, one launch for all pairs and layers.  For every
  * pair i and layer l, copies the K block (num_kv_heads * B * head_dim
  * elements) of k_caches[l] from physical block pairs[i][0] to pairs[i][1],

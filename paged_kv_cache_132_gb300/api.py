@@ -131,3 +131,26 @@ def get_device_error(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, i
     code = ctypes.c_int32(0)
     status = native.load().pa_get_device_error(_stream_ptr(stream), ctypes.byref(code))
     return int(status), int(code.value)
+
+
+def decode_noalloc(query: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                   context_lens: torch.Tensor, scale: float, *, out: torch.Tensor, max_context_len: int,
+                   num_kv_heads: Optional[int] = None, partition_size: int = 0,
+                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Decode attention through pa_decode_noalloc: for callers that must not
+    allocate device memory.  ``out`` must be given (nothing is allocated
+    here either); the workspace is the library's fixed array, so the batch must
+    fit in it (PA_ERR_WORKSPACE otherwise) and calls that overlap on the GPU
+    must be serialised by the caller."""
+    lib = native.load()
+    _check_cuda(query, k_cache, v_cache, block_tables, context_lens, out)
+    s, h, d = query.shape
+    desc = cache_desc(k_cache)
+    _require(query.dtype == k_cache.dtype and d == desc.head_dim, "query dtype/head_dim must match the pools")
+    _require(out.shape == (s, h, d) and out.dtype in DTYPE_CODE, "out is [num_seqs][num_heads][head_dim]")
+    hkv = desc.num_kv_heads if num_kv_heads is None else num_kv_heads
+    _raise(lib.pa_decode_noalloc(out.data_ptr(), DTYPE_CODE[out.dtype], query.data_ptr(), k_cache.data_ptr(),
+                                 v_cache.data_ptr(), ctypes.byref(desc), block_tables.data_ptr(),
+                                 block_tables.shape[1], context_lens.data_ptr(), s, int(max_context_len), h, hkv,
+                                 float(scale), int(partition_size), _stream_ptr(stream)), "pa_decode_noalloc")
+    return out

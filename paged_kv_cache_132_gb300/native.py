@@ -18,6 +18,7 @@ STATUS_NAMES = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED", 
                 -4: "PA_ERR_CUDA", -5: "PA_ERR_DEVICE_FAULT", -6: "PA_ERR_DEVICE_TIMEOUT"}
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_CONTEXT_LEN, DEVERR_COPY_PAIR, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # PA_NOALLOC_SCRATCH_BYTES
 
 
 class PaError(RuntimeError):
@@ -58,13 +59,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.pa_decode_workspace_size.restype = sz
         lib.pa_decode.argtypes = [vp, i32, vp, vp, vp, desc, vp, i32, vp, i32, i32, i32, i32, ctypes.c_float,
                                   i32, vp, sz, vp]
+        lib.pa_decode_noalloc.argtypes = [vp, i32, vp, vp, vp, desc, vp, i32, vp, i32, i32, i32, i32,
+                                          ctypes.c_float, i32, vp]
         lib.pa_copy_blocks.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp, i64, desc, vp]
         lib.pa_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
         lib.pa_status_string.argtypes = [ctypes.c_int]
         lib.pa_status_string.restype = ctypes.c_char_p
         lib.pa_abi_version.argtypes = []
-        for name in ("pa_reshape_and_cache", "pa_decode", "pa_copy_blocks", "pa_get_device_error",
-                     "pa_abi_version"):
+        for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_noalloc", "pa_copy_blocks",
+                     "pa_get_device_error", "pa_abi_version"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
