@@ -24,6 +24,10 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
                          uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                          const int64_t* __restrict__ slot_mapping, int64_t num_tokens, int num_kv_heads,
                          int block_size, int chunks_per_row, int64_t num_slots, int* err) {
+    // A kernel launched after this one as a programmatic dependent (the
+    // decode planning kernel) may start now; it waits for this grid's
+    // completion before anything it launches reads the pools.
+    pdl_launch_dependents();
     // Thread index -> (token t, K|V, head h, 16-byte chunk c), chunk fastest.
     const int64_t total = num_tokens * 2 * num_kv_heads * chunks_per_row;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;

@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const __grid_
         const int multi_incl = block_inclusive_scan(multi, scratch);
         const int first = carry[0] + items_incl - np;
         for (int k = 0; k < np; ++k) p.items[first + k] = make_int2(s, k);
-        if (multi) p.multi_seqs[carry[1] + multi_incl - 1] = s;
+        if (multi) p.multi_seqs[carry[1] + multi_incl - 1] = make_int2(s, np);
         __syncthreads();
         if (tid == kPlanThreads - 1) {
             carry[0] += items_incl;
@@ -101,6 +101,10 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const __grid_
         *p.num_items = carry[0] * p.num_kv_heads;
         *p.num_multi = carry[1];
     }
+    // This kernel may have been launched before the previous kernel in the
+    // stream finished (it reads nothing that kernel writes); it completes only
+    // after that kernel has, so the decode kernel's wait on it covers both.
+    pdl_wait_prerequisites();
 }
 
 template <int D>
@@ -114,39 +118,36 @@ __global__ void __launch_bounds__(kReduceThreads) decode_reduce_kernel(const __g
     const int per_seq = p.num_kv_heads * group;
     const int64_t total = (int64_t)*p.num_multi * per_seq;
     for (int64_t w = blockIdx.x * (kReduceThreads / 32) + (threadIdx.x >> 5); w < total; w += warps) {
-        const int s = p.multi_seqs[w / per_seq];
-        const int hq = (int)(w % per_seq);  // query head s*H + hq
+        const int2 sn = p.multi_seqs[w / per_seq];  // (sequence, partitions)
+        const int s = sn.x, nparts = sn.y;
+        const int hq = (int)(w % per_seq);  // query head h*G + g of sequence s
         const int h = hq / group, g = hq - h * group;
-        int ctx = p.context_lens[s];
-        ctx = ctx < 0 ? 0 : (ctx > p.ctx_cap ? p.ctx_cap : ctx);
-        const int nparts = (ctx + p.partition_size - 1) / p.partition_size;
         const int64_t base = ((int64_t)s * p.num_kv_heads + h) * p.max_parts * group + g;
-        // Max and sum over the partitions, lanes striding over them.
-        float M = NEG_INF;
-        for (int q = lane; q < nparts; q += 32) M = fmaxf(M, __ldcg(p.part_ml + 2 * (base + (int64_t)q * group)));
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float L = 0.f;
-        for (int q = lane; q < nparts; q += 32) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + 2 * (base + (int64_t)q * group)));
-            L += ml.y * exp2_approx(ml.x - M);
-        }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-        const float invL = 1.f / L;
-        // Weighted sum of the partial outputs; lane q%32 holds partition q's weight.
         float acc[VPL];
 #pragma unroll
         for (int v = 0; v < VPL; ++v) acc[v] = 0.f;
+        // Partitions in chunks of 32, lane q holding partition q's (m, l);
+        // a running max M and sum L carry the merge across chunks.
+        float M = NEG_INF, L = 0.f;
         for (int q0 = 0; q0 < nparts; q0 += 32) {
-            float wq = 0.f;
-            if (q0 + lane < nparts) {
-                const float2 ml =
-                    __ldcg(reinterpret_cast<const float2*>(p.part_ml + 2 * (base + (int64_t)(q0 + lane) * group)));
-                wq = ml.y * exp2_approx(ml.x - M) * invL;
-            }
+            float2 ml = make_float2(NEG_INF, 0.f);
+            if (q0 + lane < nparts)
+                ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + 2 * (base + (int64_t)(q0 + lane) * group)));
+            float cm = ml.x;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+            const float newM = fmaxf(M, cm);
+            const float rescale = M == NEG_INF ? 0.f : exp2_approx(M - newM);
+            const float wq = ml.y > 0.f ? ml.y * exp2_approx(ml.x - newM) : 0.f;  // l_q 2^(m_q - M)
+            float cl = wq;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) cl += __shfl_xor_sync(0xffffffffu, cl, off);
+            L = L * rescale + cl;
+            M = newM;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) acc[v] *= rescale;
             const int n = min(32, nparts - q0);
-#pragma unroll 8
+#pragma unroll 16
             for (int k = 0; k < n; ++k) {
                 const float wk = __shfl_sync(0xffffffffu, wq, k);
                 const float* src = p.part_o + (base + (int64_t)(q0 + k) * group) * D + lane * VPL;
@@ -163,15 +164,17 @@ __global__ void __launch_bounds__(kReduceThreads) decode_reduce_kernel(const __g
                 }
             }
         }
+        const float invL = 1.f / L;
         const int64_t oi = ((int64_t)s * p.num_heads + (int64_t)h * group + g) * D + lane * VPL;
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
+            const float o = acc[v] * invL;
             if (p.out_dtype == PA_F32)
-                static_cast<float*>(p.out)[oi + v] = acc[v];
+                static_cast<float*>(p.out)[oi + v] = o;
             else if (p.out_dtype == PA_F16)
-                static_cast<__half*>(p.out)[oi + v] = __float2half_rn(acc[v]);
+                static_cast<__half*>(p.out)[oi + v] = __float2half_rn(o);
             else
-                static_cast<__nv_bfloat16*>(p.out)[oi + v] = __float2bfloat16_rn(acc[v]);
+                static_cast<__nv_bfloat16*>(p.out)[oi + v] = __float2bfloat16_rn(o);
         }
     }
 }
@@ -181,10 +184,11 @@ cudaError_t launch_reduce(const DecodeParams& p, int head_dim, int group, cudaSt
     cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    // Upper bound of the warps needed; the kernel strides over the real count.
+    // One warp per (sequence, query head) up to the upper bound of the work;
+    // the kernel strides over the real count beyond 8 CTAs per SM.
     const int64_t work = (int64_t)p.num_seqs * p.num_heads;
     int64_t ctas = (work + kReduceThreads / 32 - 1) / (kReduceThreads / 32);
-    if (ctas > 4LL * sms) ctas = 4LL * sms;
+    if (ctas > 8LL * sms) ctas = 8LL * sms;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)(ctas > 0 ? ctas : 1));
     cfg.blockDim = dim3(kReduceThreads);
@@ -219,7 +223,7 @@ DecodeWorkspaceLayout decode_workspace_layout(int num_seqs, int num_heads, int m
     w.items = off;
     off = align_up(off + s * mp * sizeof(int2), 256);
     w.multi_seqs = off;
-    off = align_up(off + s * sizeof(int), 256);
+    off = align_up(off + s * sizeof(int2), 256);
     w.part_ml = off;
     off = align_up(off + s * h * mp * 2 * sizeof(float), 256);
     w.part_o = off;
@@ -233,8 +237,18 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int bl
                           const CUtensorMap* tmap_v, cudaStream_t stream) {
     const int ub = grid_items_upper_bound;
     const bool mma = variant == kDecodeMma && dtype != PA_F32 && tmap_k && tmap_v;
-    decode_plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    // The planning kernel may overlap the previous kernel in the stream (it
+    // waits for it before completing).
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_plan_kernel, p);
     if (e != cudaSuccess) return e;
     switch (dtype) {
         case PA_F32: e = launch_decode_f32(p, head_dim, block_size, group, ub, stream); break;

@@ -120,11 +120,23 @@ __device__ inline void decode_smem_init(Smem& sm, int stages, int consumer_warps
     pdl_wait_prerequisites();
 }
 
-// 2-D tiled TMA load of one box into shared memory, completed on `bar`.
-__device__ inline void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+// L2 policy for data read exactly once (the KV tiles): evict first, so that
+// the stream does not push out what is read again (partials, tables).
+__device__ inline uint64_t l2_evict_first_policy() {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    return policy;
+}
+
+// 2-D tiled TMA load of one box into shared memory, completed on `bar`, with
+// an L2 cache policy.
+__device__ inline void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                   uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(smem_addr(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_addr(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)),
+        "l"(policy)
         : "memory");
 }
 
@@ -169,6 +181,7 @@ __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm,
     uint32_t ph = 0;
     unsigned total_fills = 0;
     bool aborted = false;
+    const uint64_t stream_policy = l2_evict_first_policy();
 
     // Item metadata travels one item ahead: while item k streams, the id of
     // item k+1, its (sequence, partition) pair and its context length are
@@ -235,8 +248,8 @@ __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm,
 #pragma unroll
                     for (int slab = 0; slab < D / 64; ++slab) {
                         const int off = slab * Shape::STAGE_TOK * 128 + lane * BS * 128;
-                        tma_load_2d(sm.kv[st][0] + off, tk, slab * 64, y, &sm.full[st]);
-                        tma_load_2d(sm.kv[st][1] + off, tv, slab * 64, y, &sm.full[st]);
+                        tma_load_2d(sm.kv[st][0] + off, tk, slab * 64, y, &sm.full[st], stream_policy);
+                        tma_load_2d(sm.kv[st][1] + off, tv, slab * 64, y, &sm.full[st], stream_policy);
                     }
                 } else {
                     const int64_t tile = ((int64_t)phys * p.num_kv_heads + h) * Shape::TILE;

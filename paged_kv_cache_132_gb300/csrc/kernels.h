@@ -51,7 +51,7 @@ struct DecodeParams {
     int* num_items;            // (sequence, partition) pairs x num_kv_heads
     int2* items;               // (sequence, partition) pairs
     int* num_multi;            // sequences with more than one partition
-    int* multi_seqs;           // [num_seqs] their indices
+    int2* multi_seqs;          // [num_seqs] their (index, partition count)
     float* part_ml;            // [num_seqs * num_kv_heads * max_parts * G][2] (max, sum)
     float* part_o;             // [num_seqs * num_kv_heads * max_parts * G][head_dim]
     int* err;                  // device error word

@@ -261,7 +261,7 @@ int pa_decode(void* out, int32_t out_dtype, const void* query, const void* k_cac
     p.num_items = reinterpret_cast<int*>(ws + lay.num_items);
     p.items = reinterpret_cast<int2*>(ws + lay.items);
     p.num_multi = reinterpret_cast<int*>(ws + lay.num_multi);
-    p.multi_seqs = reinterpret_cast<int*>(ws + lay.multi_seqs);
+    p.multi_seqs = reinterpret_cast<int2*>(ws + lay.multi_seqs);
     p.part_ml = reinterpret_cast<float*>(ws + lay.part_ml);
     p.part_o = reinterpret_cast<float*>(ws + lay.part_o);
     p.err = err;
