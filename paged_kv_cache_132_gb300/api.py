@@ -96,8 +96,8 @@ def decode(query: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
         out = torch.empty((s, h, d), dtype=out_dtype, device=query.device)
     _check_cuda(out)
     _require(out.shape == (s, h, d) and out.dtype in DTYPE_CODE, "out is [num_seqs][num_heads][head_dim]")
-    need = decode_workspace_size(s, h, max_context_len, partition_size, d)
     if workspace is None:
+        need = decode_workspace_size(s, h, max_context_len, partition_size, d)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=query.device)
     _check_cuda(workspace)
     _raise(lib.pa_decode(out.data_ptr(), DTYPE_CODE[out.dtype], query.data_ptr(), k_cache.data_ptr(),

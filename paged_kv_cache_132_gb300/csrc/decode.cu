@@ -179,11 +179,7 @@ __global__ void __launch_bounds__(kReduceThreads) decode_reduce_kernel(const __g
     }
 }
 
-cudaError_t launch_reduce(const DecodeParams& p, int head_dim, int group, cudaStream_t stream) {
-    int dev = 0, sms = 0;
-    cudaError_t e;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+cudaError_t launch_reduce(const DecodeParams& p, int head_dim, int group, int sms, cudaStream_t stream) {
     // One warp per (sequence, query head) up to the upper bound of the work;
     // the kernel strides over the real count beyond 8 CTAs per SM.
     const int64_t work = (int64_t)p.num_seqs * p.num_heads;
@@ -201,6 +197,17 @@ cudaError_t launch_reduce(const DecodeParams& p, int head_dim, int group, cudaSt
     if (head_dim == 64) return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<64>, p, group);
     if (head_dim == 128) return cudaLaunchKernelEx(&cfg, decode_reduce_kernel<128>, p, group);
     return cudaErrorNotSupported;
+}
+
+int device_sm_count() {
+    constexpr int kMaxDevices = 64;
+    static int cached[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    int n = __atomic_load_n(&cached[dev], __ATOMIC_ACQUIRE);
+    if (n == 0 && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+        __atomic_store_n(&cached[dev], n, __ATOMIC_RELEASE);
+    return n;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -264,7 +271,11 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int bl
     }
     if (e != cudaSuccess) return e;
     // With a single partition per sequence every output is already final.
-    if (p.max_parts > 1) e = launch_reduce(p, head_dim, group, stream);
+    if (p.max_parts > 1) {
+        const int sms = device_sm_count();
+        if (sms <= 0) return cudaErrorInvalidDevice;
+        e = launch_reduce(p, head_dim, group, sms, stream);
+    }
     return e;
 }
 

@@ -394,19 +394,30 @@ __device__ inline void consumer_abort(const DecodeParams& p, int* abort_flag, in
     }
 }
 
-// Occupancy-sized persistent launch of `kernel`.
+// Occupancy-sized persistent launch of `kernel`.  The shared-memory opt-in
+// and the resident-CTA count are set up once per (kernel, device) and cached.
 template <class Shape, typename Kernel, typename... Args>
 cudaError_t launch_persistent(Kernel kernel, int items_upper_bound, cudaStream_t stream, Args... args) {
     constexpr int smem = Shape::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    constexpr int kMaxDevices = 64;
+    static int resident[kMaxDevices];  // SMs x CTAs per SM; 0 = not set up yet
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, occ = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, Shape::THREADS, smem)) != cudaSuccess)
-        return e;
-    if (occ < 1) return cudaErrorInvalidConfiguration;
-    int grid = sms * occ;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int slots = __atomic_load_n(&resident[dev], __ATOMIC_ACQUIRE);
+    if (slots == 0) {
+        int sms = 0, occ = 0;
+        if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+            return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, Shape::THREADS, smem)) != cudaSuccess)
+            return e;
+        if (occ < 1) return cudaErrorInvalidConfiguration;
+        slots = sms * occ;
+        __atomic_store_n(&resident[dev], slots, __ATOMIC_RELEASE);
+    }
+    int grid = slots;
     if (items_upper_bound < grid) grid = items_upper_bound > 0 ? items_upper_bound : 1;
     // Launched as a programmatic dependent of the planning kernel.
     cudaLaunchConfig_t cfg{};
