@@ -179,7 +179,9 @@ __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm,
 
     int st = 0;
     uint32_t ph = 0;
-    unsigned total_fills = 0;
+    uint32_t filled = 0;        // bit j: stage j was filled at least once
+    uint32_t fill_parity = 0;   // bit j: parity of stage j's last fill
+    bool drop_next_fill = (p.debug_flags & kDebugDropFirstFill) != 0;
     bool aborted = false;
     const uint64_t stream_policy = l2_evict_first_policy();
 
@@ -227,41 +229,48 @@ __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm,
                 aborted = true;
                 break;
             }
-            if (lane == 0) {
-                StageMeta m;
-                m.item = item;
-                m.seq = s;
-                m.kv_head = h;
-                m.part = part;
-                m.nparts = nparts;
-                m.t0 = t0;
-                m.te = te;
-                m.first = c == 0;
-                m.last = c == nst - 1;
-                sm.meta[st] = m;
-                mbar_arrive_expect_tx(&sm.full[st], bytes);
-            }
-            __syncwarp();
-            if (ok) {
-                if constexpr (TENSOR) {
-                    const int y = (int)(((int64_t)phys * p.num_kv_heads + h) * BS);
-#pragma unroll
-                    for (int slab = 0; slab < D / 64; ++slab) {
-                        const int off = slab * Shape::STAGE_TOK * 128 + lane * BS * 128;
-                        tma_load_2d(sm.kv[st][0] + off, tk, slab * 64, y, &sm.full[st], stream_policy);
-                        tma_load_2d(sm.kv[st][1] + off, tv, slab * 64, y, &sm.full[st], stream_policy);
-                    }
-                } else {
-                    const int64_t tile = ((int64_t)phys * p.num_kv_heads + h) * Shape::TILE;
-                    bulk_copy_g2s(sm.kv[st][0] + lane * Shape::TILE, kbase + tile, Shape::TILE, &sm.full[st]);
-                    bulk_copy_g2s(sm.kv[st][1] + lane * Shape::TILE, vbase + tile, Shape::TILE, &sm.full[st]);
+            // Test hook: leave this stage unfilled (no copies, no arrival);
+            // the rest of the loop body runs as usual.  Uniform across lanes.
+            const bool drop = drop_next_fill;
+            drop_next_fill = false;
+            if (!drop) {
+                if (lane == 0) {
+                    StageMeta m;
+                    m.item = item;
+                    m.seq = s;
+                    m.kv_head = h;
+                    m.part = part;
+                    m.nparts = nparts;
+                    m.t0 = t0;
+                    m.te = te;
+                    m.first = c == 0;
+                    m.last = c == nst - 1;
+                    sm.meta[st] = m;
+                    mbar_arrive_expect_tx(&sm.full[st], bytes);
                 }
+                __syncwarp();
+                if (ok) {
+                    if constexpr (TENSOR) {
+                        const int y = (int)(((int64_t)phys * p.num_kv_heads + h) * BS);
+#pragma unroll
+                        for (int slab = 0; slab < D / 64; ++slab) {
+                            const int off = slab * Shape::STAGE_TOK * 128 + lane * BS * 128;
+                            tma_load_2d(sm.kv[st][0] + off, tk, slab * 64, y, &sm.full[st], stream_policy);
+                            tma_load_2d(sm.kv[st][1] + off, tv, slab * 64, y, &sm.full[st], stream_policy);
+                        }
+                    } else {
+                        const int64_t tile = ((int64_t)phys * p.num_kv_heads + h) * Shape::TILE;
+                        bulk_copy_g2s(sm.kv[st][0] + lane * Shape::TILE, kbase + tile, Shape::TILE, &sm.full[st]);
+                        bulk_copy_g2s(sm.kv[st][1] + lane * Shape::TILE, vbase + tile, Shape::TILE, &sm.full[st]);
+                    }
+                }
+                if (c == 0 && lane == 31) {
+                    const int64_t qoff = ((int64_t)s * p.num_heads + (int64_t)h * G) * D * Shape::E;
+                    bulk_copy_g2s(sm.q[st], qbase + qoff, Shape::QBYTES, &sm.full[st]);
+                }
+                filled |= 1u << st;
+                fill_parity = (fill_parity & ~(1u << st)) | (ph << st);
             }
-            if (c == 0 && lane == 31) {
-                const int64_t qoff = ((int64_t)s * p.num_heads + (int64_t)h * G) * D * Shape::E;
-                bulk_copy_g2s(sm.q[st], qbase + qoff, Shape::QBYTES, &sm.full[st]);
-            }
-            ++total_fills;
             if (++st == Shape::NSTAGE) {
                 st = 0;
                 ph ^= 1u;
@@ -289,7 +298,8 @@ __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm,
                 sm.meta[st].item = -1;
                 mbar_arrive(&sm.full[st]);
             }
-            ++total_fills;
+            filled |= 1u << st;
+            fill_parity = (fill_parity & ~(1u << st)) | (ph << st);
         } else {
             aborted = true;
         }
@@ -300,13 +310,12 @@ __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm,
     }
     // This CTA takes no more work: the reduce kernel may start launching.
     pdl_launch_dependents();
-    // Drain: every copy this warp issued must land before the CTA exits.
+    // Drain: every copy this warp issued must land before the CTA exits --
+    // wait for the last fill of every stage (bounded).
     if (lane == 0) {
         for (int j = 0; j < Shape::NSTAGE; ++j) {
-            const unsigned fills =
-                total_fills > (unsigned)j ? (total_fills - j + Shape::NSTAGE - 1) / Shape::NSTAGE : 0u;
-            if (fills == 0) continue;
-            if (!mbar_wait_bounded(&sm.full[j], (fills - 1u) & 1u, p.wait_limit_ns))
+            if (!(filled & (1u << j))) continue;
+            if (!mbar_wait_bounded(&sm.full[j], (fill_parity >> j) & 1u, p.wait_limit_ns))
                 set_error(p.err, PA_DEVERR_TIMEOUT);
         }
     }

@@ -179,7 +179,8 @@ __device__ void simt_consumer(const DecodeParams& p, typename DecodeShape<T, D, 
             st = 0;
             ph ^= 1u;
         }
-        if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) break;
+        // Another warp's wait ran out: stop too (decided for the whole warp).
+        if (__any_sync(kFullMask, *reinterpret_cast<volatile int*>(&sm.abort_flag) != 0)) break;
     }
 }
 

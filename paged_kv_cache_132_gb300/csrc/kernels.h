@@ -56,7 +56,13 @@ struct DecodeParams {
     float* part_o;             // [num_seqs * num_kv_heads * max_parts * G][head_dim]
     int* err;                  // device error word
     unsigned long long wait_limit_ns;
+    int debug_flags;           // kDebugDropFirstFill: tests of the bounded waits
 };
+
+// Test hook (environment variable PA_DEBUG_DROP_FIRST_FILL=1): every decode
+// CTA leaves its first pipeline stage unfilled, so that its consumers' bounded
+// wait runs out and the call reports PA_DEVERR_TIMEOUT.
+constexpr int kDebugDropFirstFill = 1;
 
 struct DecodeWorkspaceLayout {
     size_t next_item, num_items, num_multi, items, multi_seqs, part_ml, part_o, total;

@@ -266,6 +266,8 @@ int pa_decode(void* out, int32_t out_dtype, const void* query, const void* k_cac
     p.part_o = reinterpret_cast<float*>(ws + lay.part_o);
     p.err = err;
     p.wait_limit_ns = wait_limit_ns();
+    const char* drop = std::getenv("PA_DEBUG_DROP_FIRST_FILL");
+    p.debug_flags = (drop && drop[0] == '1') ? pa::kDebugDropFirstFill : 0;
 
     pa::DecodeVariant variant = requested_variant();
     CUtensorMap tmap_k, tmap_v;
