@@ -244,19 +244,22 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int bl
                           const CUtensorMap* tmap_v, cudaStream_t stream) {
     const int ub = grid_items_upper_bound;
     const bool mma = variant == kDecodeMma && dtype != PA_F32 && tmap_k && tmap_v;
-    // The planning kernel may overlap the previous kernel in the stream (it
-    // waits for it before completing).
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(1);
-    cfg.blockDim = dim3(kPlanThreads);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_plan_kernel, p);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (p.direct_items == 0) {
+        // The planning kernel may overlap the previous kernel in the stream (it
+        // waits for it before completing).
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(kPlanThreads);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, decode_plan_kernel, p);
+        if (e != cudaSuccess) return e;
+    }
     switch (dtype) {
         case PA_F32: e = launch_decode_f32(p, head_dim, block_size, group, ub, stream); break;
         case PA_F16:

@@ -76,6 +76,7 @@ struct DecodeShape {
     static constexpr int KV_STAGE_BYTES = STAGE_TOK * ROW;
     static constexpr int QBYTES = G * D * E;
     static_assert(QBYTES % 16 == 0, "the q tile is one bulk copy");
+    static constexpr bool INTERLEAVED = interleaved_stage(D, BS);
     static_assert(D % 128 == 0 || D == 64, "the merge warp stores 4 consecutive dims per lane");
 
     struct Smem {
@@ -140,6 +141,33 @@ __device__ inline void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x
         : "memory");
 }
 
+// 3-D variant: box {64 elements, 2 slabs, BS rows} of the view [rows][2][64].
+__device__ inline void tma_load_3d(void* smem_dst, const CUtensorMap* map, int x, int z, int y, uint64_t* bar,
+                                   uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        ::"r"(smem_addr(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(z), "r"(y),
+        "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Shared-memory address of 16-byte chunk c of stage row r, as the tensor
+// copies (128-byte swizzle: chunk k of a 128-byte line L sits at k ^ (L % 8))
+// laid the stage out.
+//   slab layout:        line (c/8, r) at (c/8)*STAGE_TOK*128 + r*128, L = r
+//   interleaved layout: line (r, c/8) at r*256 + (c/8)*128,            L = 2r + c/8
+template <class Shape>
+__device__ inline uint32_t stage_chunk_addr(uint32_t base, int r, int c) {
+    const int slab = c >> 3, k = c & 7;
+    if constexpr (Shape::INTERLEAVED) {
+        const int line = 2 * r + slab;
+        return base + (uint32_t)(line * 128 + ((k ^ (line & 7)) << 4));
+    } else {
+        return base + (uint32_t)(slab * Shape::STAGE_TOK * 128 + r * 128 + ((k ^ (r & 7)) << 4));
+    }
+}
+
 __device__ inline void store_out4(void* out, int dtype, int64_t index, float4 v) {
     if (dtype == PA_F32) {
         *reinterpret_cast<float4*>(static_cast<float*>(out) + index) = v;
@@ -171,7 +199,8 @@ template <class Shape, int BS, int G, bool TENSOR>
 __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm, int lane, const CUtensorMap* tk,
                                 const CUtensorMap* tv) {
     constexpr int D = Shape::ROW / Shape::E;
-    const int num_items = *p.num_items;
+    const bool direct = p.direct_items > 0;
+    const int num_items = direct ? p.direct_items : *p.num_items;
     const int part_size = p.partition_size;
     const char* kbase = static_cast<const char*>(p.k_cache);
     const char* vbase = static_cast<const char*>(p.v_cache);
@@ -188,17 +217,28 @@ __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm,
     // Item metadata travels one item ahead: while item k streams, the id of
     // item k+1, its (sequence, partition) pair and its context length are
     // already being fetched, so a new item starts without dependent loads.
-    auto item_pair = [&](int it) { return it < num_items ? p.items[it / p.num_kv_heads] : make_int2(0, 0); };
-    int item = 0;
-    if (lane == 0) item = atomicAdd(p.next_item, 1);
-    item = __shfl_sync(kFullMask, item, 0);
+    auto item_pair = [&](int it) {
+        if (it >= num_items) return make_int2(0, 0);
+        return direct ? make_int2(it / p.num_kv_heads, 0) : p.items[it / p.num_kv_heads];
+    };
+    // Work items: from the device counter, or (direct) a fixed stride.
+    auto take_item = [&](int previous) {
+        int it = 0;
+        if (direct)
+            it = previous < 0 ? (int)blockIdx.x : previous + (int)gridDim.x;
+        else if (lane == 0)
+            it = atomicAdd(p.next_item, 1);
+        return it;
+    };
+    int item = __shfl_sync(kFullMask, take_item(-1), 0);
     int2 sp = item_pair(item);
     int ctx_raw = item < num_items ? __ldg(p.context_lens + sp.x) : 0;
     while (item < num_items) {
-        int next = 0;
-        if (lane == 0) next = atomicAdd(p.next_item, 1);
+        int next = take_item(item);
         const int h = item - (item / p.num_kv_heads) * p.num_kv_heads;
         const int s = sp.x, part = sp.y;
+        if (direct && lane == 0 && h == 0 && (ctx_raw < 0 || ctx_raw > p.ctx_cap))
+            set_error(p.err, PA_DEVERR_CONTEXT_LEN);
         const int ctx = ctx_raw < 0 ? 0 : (ctx_raw > p.ctx_cap ? p.ctx_cap : ctx_raw);
         const int nparts = ctx == 0 ? 1 : (ctx + part_size - 1) / part_size;
         const int tb = part * part_size;
@@ -250,7 +290,11 @@ __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm,
                 }
                 __syncwarp();
                 if (ok) {
-                    if constexpr (TENSOR) {
+                    if constexpr (TENSOR && Shape::INTERLEAVED) {
+                        const int y = (int)(((int64_t)phys * p.num_kv_heads + h) * BS);
+                        tma_load_3d(sm.kv[st][0] + lane * Shape::TILE, tk, 0, 0, y, &sm.full[st], stream_policy);
+                        tma_load_3d(sm.kv[st][1] + lane * Shape::TILE, tv, 0, 0, y, &sm.full[st], stream_policy);
+                    } else if constexpr (TENSOR) {
                         const int y = (int)(((int64_t)phys * p.num_kv_heads + h) * BS);
 #pragma unroll
                         for (int slab = 0; slab < D / 64; ++slab) {

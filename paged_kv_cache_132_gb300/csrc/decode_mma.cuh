@@ -6,9 +6,10 @@
 // the G heads on the M dimension (rows G..15 are zero), fp32 accumulation.
 //
 //  * Q K^T: the A fragments of q are loaded once per item; the B fragments of
-//    K come from the stage with ldmatrix.  The stage is filled by 2-D tensor
-//    copies with 128-byte swizzle (row r's 16-byte chunk c sits at c ^ (r%8)),
-//    so the eight rows an ldmatrix reads fall in eight different bank groups.
+//    K come from the stage with ldmatrix.  The stage is filled by tensor
+//    copies with 128-byte swizzle (a line's 16-byte chunk k sits at k ^ (line
+//    % 8)), so the eight rows an ldmatrix reads fall in eight different bank
+//    groups (four with the interleaved layout of 8-token blocks).
 //  * The accumulator of S has exactly the register layout of the A operand of
 //    P V (row g = lane/4, tokens 2j, 2j+1 and 8+2j, 8+2j+1 for j = lane%4),
 //    so the softmax runs in registers and P feeds the next MMA directly.
@@ -70,13 +71,6 @@ __device__ inline void ldmatrix_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
-}
-
-// Shared-memory address of 16-byte chunk c (of D*2/16) of stage row r in
-// the swizzled stage layout written by the tensor copies.
-template <int STAGE_TOK>
-__device__ inline uint32_t swizzled_chunk(uint32_t stage_base, int r, int c) {
-    return stage_base + (uint32_t)((c >> 3) * STAGE_TOK * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 template <typename T, int D, int BS, int G>
@@ -151,7 +145,7 @@ __device__ void mma_consumer(const DecodeParams& p, typename DecodeShape<T, D, B
                 for (int t = 0; t < 2; ++t) {
                     uint32_t b0, b1, b2, b3;
                     ldmatrix_x4(b0, b1, b2, b3,
-                                swizzled_chunk<S::STAGE_TOK>(kst, row0 + t * 8 + (lane & 7), kp * 4 + (lane >> 3)));
+                                stage_chunk_addr<S>(kst, row0 + t * 8 + (lane & 7), kp * 4 + (lane >> 3)));
                     Ops::mma(sacc[t], qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, b0, b1);
                     Ops::mma(sodd[t], qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, b2, b3);
                 }
@@ -206,8 +200,8 @@ __device__ void mma_consumer(const DecodeParams& p, typename DecodeShape<T, D, B
             for (int dp = 0; dp < NT / 2; ++dp) {
                 uint32_t v0, v1, v2, v3;
                 ldmatrix_x4_trans(v0, v1, v2, v3,
-                                  swizzled_chunk<S::STAGE_TOK>(vst, row0 + (lane & 7) + ((lane >> 3) & 1) * 8,
-                                                               2 * dp + (lane >> 4)));
+                                  stage_chunk_addr<S>(vst, row0 + (lane & 7) + ((lane >> 3) & 1) * 8,
+                                                      2 * dp + (lane >> 4)));
                 if (partial) {
                     v0 &= mask_lo;
                     v2 &= mask_lo;

@@ -57,6 +57,11 @@ struct DecodeParams {
     int* err;                  // device error word
     unsigned long long wait_limit_ns;
     int debug_flags;           // kDebugDropFirstFill: tests of the bounded waits
+    // > 0: every sequence fits one partition and no planning kernel ran; item
+    // i is (sequence i / num_kv_heads, partition 0), CTAs take items
+    // blockIdx.x, blockIdx.x + gridDim.x, ...; the decode kernel checks the
+    // context lengths itself.  0: the planning kernel wrote the work list.
+    int direct_items;
 };
 
 // Test hook (environment variable PA_DEBUG_DROP_FIRST_FILL=1): every decode
@@ -73,6 +78,14 @@ DecodeWorkspaceLayout decode_workspace_layout(int num_seqs, int num_heads, int m
 // Tokens per pipeline stage of the decode kernel for this head_dim/element
 // size; partition sizes are multiples of it.
 int decode_stage_tokens(int head_dim, int elem_bytes);
+
+// Stage layout of the tensor-core decode kernel.  A (block, head) tile of
+// head_dim 128 is two 128-byte column slabs per row.  With 8-token blocks a
+// tile is 2 KiB and is fetched as ONE box of a 3-D view [rows][2][64] --
+// rows interleaved in shared memory, 256 bytes apart -- because 1 KiB boxes
+// cost more per byte than the bandwidth allows; otherwise each slab is its
+// own box of the 2-D view [rows][d] and the stage keeps the slabs apart.
+constexpr bool interleaved_stage(int head_dim, int block_size) { return head_dim == 128 && block_size == 8; }
 
 // Which decode consumer runs: the tensor-core one (16-bit pools, needs the
 // two tensor maps) or the CUDA-core one (every dtype).

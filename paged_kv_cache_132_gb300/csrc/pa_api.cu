@@ -123,15 +123,29 @@ bool encode_pool_map(CUtensorMap* map, const void* base, int dtype, const pa::Po
     if (rows <= 0 || rows >= (1LL << 31) || shape.head_dim % 64 != 0) return false;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)shape.head_dim, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)shape.head_dim * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)shape.block_size};
-    const cuuint32_t elem_strides[2] = {1, 1};
+    const CUtensorMapDataType type =
+        dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     std::memset(map, 0, sizeof(*map));
-    const CUresult r = encode(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                              2, const_cast<void*>(base), dims, strides, box, elem_strides,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    if (pa::interleaved_stage(shape.head_dim, shape.block_size)) {
+        // [rows][2 slabs][64]: one box = one whole (block, head) tile.
+        const cuuint64_t dims[3] = {64, 2, (cuuint64_t)rows};
+        const cuuint64_t strides[2] = {128, 256};
+        const cuuint32_t box[3] = {64, 2, (cuuint32_t)shape.block_size};
+        const cuuint32_t elem_strides[3] = {1, 1, 1};
+        r = encode(map, type, 3, const_cast<void*>(base), dims, strides, box, elem_strides,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        // [rows][d]: one box = one 64-element column slab of a tile.
+        const cuuint64_t dims[2] = {(cuuint64_t)shape.head_dim, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)shape.head_dim * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)shape.block_size};
+        const cuuint32_t elem_strides[2] = {1, 1};
+        r = encode(map, type, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS;
 }
 
@@ -268,6 +282,8 @@ int pa_decode(void* out, int32_t out_dtype, const void* query, const void* k_cac
     p.wait_limit_ns = wait_limit_ns();
     const char* drop = std::getenv("PA_DEBUG_DROP_FIRST_FILL");
     p.debug_flags = (drop && drop[0] == '1') ? pa::kDebugDropFirstFill : 0;
+    // Every context fits one partition: no planning kernel, items are implicit.
+    p.direct_items = max_parts == 1 ? (int)items_ub : 0;
 
     pa::DecodeVariant variant = requested_variant();
     CUtensorMap tmap_k, tmap_v;

@@ -233,3 +233,35 @@ def test_repeated_calls_reuse_workspace(kernel):
     for o in outs:
         assert torch.equal(o, outs[0])
     assert torch.max(torch.abs(outs[0] - first)) < ATOL
+
+
+def test_step_captured_in_cuda_graph(kernel):
+    """The step's calls can be captured in a CUDA graph (no allocation, no
+    synchronisation inside them) and the replay gives the same outputs."""
+    w = workloads.make("llama8b", device="cuda", num_seqs=32)
+    mc = int(w.context_lens.max())
+    k, v = w.k_cache.clone(), w.v_cache.clone()
+    ws = torch.empty(api.decode_workspace_size(w.num_seqs, w.num_heads, mc, 0, w.head_dim), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty(w.num_seqs, w.num_heads, w.head_dim, device="cuda")
+
+    def step():
+        api.reshape_and_cache(w.new_key, w.new_value, k, v, w.slot_mapping)
+        api.decode(w.query, k, v, w.block_tables, w.context_lens, w.scale, out=out, max_context_len=mc,
+                   workspace=ws)
+
+    step()
+    torch.cuda.synchronize()
+    ref = out.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            step()
+    out.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert api.get_device_error() == (0, 0)
+    assert torch.equal(out, ref)
