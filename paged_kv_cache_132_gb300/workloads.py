@@ -277,3 +277,88 @@ def make(name: str, device="cpu", *, block_size: Optional[int] = None, num_seqs:
                      partition_size=0, seed=seed, device=device,
                      notes={"prompts": prompts, "samples": samples, "prompt_len": prompt_len,
                             "unique_blocks_used": used})
+
+
+# ---------------------------------------------------------------------------
+# beam search: sharing that changes every step
+# ---------------------------------------------------------------------------
+@dataclass
+class BeamStep:
+    """One decode step of beam search: copy-on-write pairs, then the new
+    tokens' K/V and slots, then attention for every live beam."""
+    copy_pairs: torch.Tensor     # int64 [n][2]
+    slot_mapping: torch.Tensor   # int64 [beams]
+    new_key: torch.Tensor        # [beams][Hkv][d]
+    new_value: torch.Tensor
+    block_tables: torch.Tensor   # int32 [beams][max_blocks] after this step
+    context_lens: torch.Tensor   # int32 [beams]
+    query: torch.Tensor          # [beams][H][d]
+    freed_blocks: int            # blocks returned to the pool at this step
+
+
+@dataclass
+class BeamSearchTrace:
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    dtype: torch.dtype
+    num_blocks: int
+    scale: float
+    k_cache: torch.Tensor        # pool after the prompt, before step 0
+    v_cache: torch.Tensor
+    steps: List[BeamStep]
+
+
+def beam_search(*, beams: int = 4, prompt_len: int = 45, steps: int = 40, num_heads: int = 8,
+                num_kv_heads: int = 2, head_dim: int = 64, block_size: int = 4, dtype=torch.bfloat16,
+                seed: int = SEED_BASE + 10, device="cpu") -> BeamSearchTrace:
+    """A seeded beam-search trace ("PagedAttention 论文精读笔记", §6.2, Fig. 9).
+
+    The prompt is stored once and shared by all beams.  At every step each of
+    the `beams` new candidates picks a parent among the current beams
+    (uniformly, with replacement): parents picked several times are forked
+    (blocks shared, refcount + 1), beams not picked die and their blocks are
+    released (freed when the count reaches zero).  Every candidate then
+    appends its token; a shared last block is first copied (copy-on-write)."""
+    gen_cpu = torch.Generator().manual_seed(seed)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    per_beam = blocks_needed(prompt_len + steps + 1, block_size)
+    num_blocks = blocks_needed(prompt_len, block_size) + beams * (per_beam + 2)
+    mgr = BlockManager(num_blocks, block_size, _permutation(num_blocks, gen_cpu))
+    mgr.add_sequence(0, prompt_len)
+    prompt_slots = mgr.prompt_slots(0)
+    keys = _normal((prompt_len, num_kv_heads, head_dim), dtype, gen, device)
+    values = _normal((prompt_len, num_kv_heads, head_dim), dtype, gen, device)
+    k_cache = _pool_from_tokens(keys, prompt_slots, num_blocks, block_size)
+    v_cache = _pool_from_tokens(values, prompt_slots, num_blocks, block_size)
+    live = [0]
+    next_id = 1
+    out_steps = []
+    for _ in range(steps):
+        free_before = mgr.num_free()
+        parents = torch.randint(0, len(live), (beams,), generator=gen_cpu).tolist()
+        new_live = []
+        for p in parents:
+            mgr.fork(live[p], next_id)
+            new_live.append(next_id)
+            next_id += 1
+        for seq in live:
+            mgr.free_sequence(seq)
+        freed = mgr.num_free() - free_before
+        live = new_live
+        slots = [mgr.append_token(seq) for seq in live]
+        pairs = mgr.take_copies()
+        out_steps.append(BeamStep(
+            copy_pairs=torch.tensor(pairs, dtype=torch.int64, device=device).reshape(-1, 2),
+            slot_mapping=torch.tensor(slots, dtype=torch.int64, device=device),
+            new_key=_normal((beams, num_kv_heads, head_dim), dtype, gen, device),
+            new_value=_normal((beams, num_kv_heads, head_dim), dtype, gen, device),
+            block_tables=_tables_tensor([mgr.table(seq) for seq in live]).to(device),
+            context_lens=torch.tensor([mgr.length(seq) for seq in live], dtype=torch.int32, device=device),
+            query=_normal((beams, num_heads, head_dim), dtype, gen, device),
+            freed_blocks=freed))
+    return BeamSearchTrace(num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                           block_size=block_size, dtype=dtype, num_blocks=num_blocks,
+                           scale=1.0 / math.sqrt(head_dim), k_cache=k_cache, v_cache=v_cache, steps=out_steps)

@@ -85,3 +85,30 @@ def test_llama_lengths_distribution():
     ctx = torch.clamp(torch.round(draw), 16, 8192)
     assert 600 < float(ctx.median()) < 1700
     assert ctx.min() >= 16 and ctx.max() <= 8192
+
+
+def test_beam_search_trace_bookkeeping():
+    t = workloads.beam_search(beams=4, prompt_len=45, steps=40, block_size=4)
+    b = t.block_size
+    prev_tables = None
+    total_copies = 0
+    for i, st in enumerate(t.steps):
+        ctx = st.context_lens.tolist()
+        assert ctx == [45 + i + 1] * 4
+        slots = st.slot_mapping.tolist()
+        assert len(set(slots)) == len(slots), "two beams write the same slot"
+        tables = st.block_tables
+        for beam, slot in enumerate(slots):
+            pos = ctx[beam] - 1
+            assert slot == int(tables[beam, pos // b]) * b + pos % b
+        pairs = st.copy_pairs.tolist()
+        total_copies += len(pairs)
+        dsts = [d for _, d in pairs]
+        assert len(set(dsts)) == len(dsts)
+        assert not set(dsts) & {s for s, _ in pairs}
+        if prev_tables is not None:
+            # a copied block was shared by the previous step's beams
+            prev_blocks = set(prev_tables[prev_tables >= 0].tolist())
+            assert all(src in prev_blocks for src, _ in pairs)
+        prev_tables = tables
+    assert total_copies > 0 and sum(st.freed_blocks for st in t.steps) > 0

@@ -265,3 +265,48 @@ def test_step_captured_in_cuda_graph(kernel):
     torch.cuda.synchronize()
     assert api.get_device_error() == (0, 0)
     assert torch.equal(out, ref)
+
+
+def test_many_sequences():
+    """3000 sequences: the planning kernel's scan spans several 1024-sequence
+    chunks, and the decode kernel several waves of work items."""
+    g = torch.Generator().manual_seed(31)
+    lens = torch.randint(0, 700, (3000,), generator=g).tolist()
+    w = workloads.custom(lens, num_heads=8, num_kv_heads=2, head_dim=64, block_size=16, dtype=torch.bfloat16,
+                         device="cuda", seed=313)
+    for partition in (0, 128):
+        _check_step(w, partition_size=partition)
+
+
+def test_longest_context():
+    """One 131072-token sequence next to short ones (256 partitions of 512)."""
+    w = workloads.custom([131072, 3, 700], num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                         dtype=torch.bfloat16, device="cuda", seed=314)
+    _check_step(w, partition_size=512)
+
+
+def test_beam_search_trace(kernel):
+    """Beam search with forks, deaths and copy-on-write at every step: the
+    pools match the oracle bit for bit after every step, and every step's
+    attention matches within the bar."""
+    import oracle as O
+
+    t = workloads.beam_search(beams=4, prompt_len=45, steps=40, block_size=8, num_heads=8, num_kv_heads=2,
+                              head_dim=64, dtype=torch.bfloat16, device="cuda")
+    assert sum(st.copy_pairs.shape[0] for st in t.steps) > 0
+    orc = O.get()
+    k, v = t.k_cache.clone(), t.v_cache.clone()
+    kb, vb = bits(t.k_cache).copy(), bits(t.v_cache).copy()
+    for st in t.steps:
+        if st.copy_pairs.numel():
+            api.copy_blocks([k], [v], st.copy_pairs)
+            orc.copy_blocks([kb], [vb], st.copy_pairs.cpu().numpy())
+        api.reshape_and_cache(st.new_key, st.new_value, k, v, st.slot_mapping)
+        orc.reshape_and_cache(bits(st.new_key), bits(st.new_value), kb, vb, st.slot_mapping.cpu().numpy())
+        out = api.decode(st.query, k, v, st.block_tables, st.context_lens, t.scale,
+                         max_context_len=int(st.context_lens.max()))
+        assert api.get_device_error() == (0, 0)
+        assert pools_equal(k, kb) and pools_equal(v, vb)
+        ref = orc.decode(bits(st.query), kb, vb, O.BF16, st.block_tables.cpu().numpy(),
+                         st.context_lens.cpu().numpy(), t.num_kv_heads, t.scale)
+        assert max_violation(out, ref) <= 0.0
