@@ -56,11 +56,12 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle leg")
-    ap.add_argument("--workload", choices=list(workloads.WORKLOADS), default=WORKLOAD,
+    ap.add_argument("--workload", choices=list(workloads.WORKLOADS) + ["beam_search"], default=WORKLOAD,
                     help="which synthetic workload one step runs over (default: the Llama-8B-shaped batch)")
     ap.add_argument("--block-size", type=int, default=16, help="long_context sweep point (8, 16 or 32)")
     ap.add_argument("--partition-size", type=int, default=None,
                     help="split-KV partition (default: the workload's, else 512)")
+    ap.add_argument("--beam-steps", type=int, default=16, help="steps of the beam_search trace")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="first n sequences only (a smaller case of the same distribution, for profiling)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) leg")
@@ -305,6 +306,43 @@ def graph_time_us(fn, reps, stream):
     return 1e3 * s.elapsed_time(e) / reps
 
 
+def swap_rows(w, stream, pairs_n=2048):
+    """Swap-out (GPU -> page-locked host) and swap-in of 2048 random blocks of
+    the workload's pool in one pa_swap_blocks launch each, against one
+    cudaMemcpyAsync per K and per V block (both timed from CUDA graphs).
+    GB/s = bytes moved (each block once) / time."""
+    g = torch.Generator().manual_seed(7)
+    n = min(pairs_n, w.num_blocks)
+    src = torch.randperm(w.num_blocks, generator=g)[:n]
+    hk = torch.empty((n,) + tuple(w.k_cache.shape[1:]), dtype=w.k_cache.dtype).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    out_pairs = torch.stack([src, torch.arange(n)], dim=1).contiguous().cuda()
+    in_pairs = torch.stack([torch.arange(n), src], dim=1).contiguous().cuda()
+    moved = 2 * n * w.k_cache[0].numel() * w.k_cache.element_size()
+    out_us = graph_time_us(lambda: api.swap_blocks([w.k_cache], [w.v_cache], [hk], [hv], out_pairs), 5, stream)
+    in_us = graph_time_us(lambda: api.swap_blocks([hk], [hv], [w.k_cache], [w.v_cache], in_pairs), 5, stream)
+    src_list = src.tolist()
+
+    def per_block_out():
+        for j, b in enumerate(src_list):
+            hk[j].copy_(w.k_cache[b], non_blocking=True)
+            hv[j].copy_(w.v_cache[b], non_blocking=True)
+
+    memcpy_us = graph_time_us(per_block_out, 1, stream)
+    # Reference: the same bytes as two contiguous device -> host copies.
+    dk, dv = w.k_cache[:n], w.v_cache[:n]
+    contiguous_us = graph_time_us(lambda: (hk.copy_(dk, non_blocking=True), hv.copy_(dv, non_blocking=True)), 5,
+                                  stream)
+    status, code = api.get_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error {status} ({code:#x}) in the swap rows")
+    return {"swap_out_us": out_us, "swap_out_gbs": moved / (out_us * 1e-6) / 1e9,
+            "swap_in_us": in_us, "swap_in_gbs": moved / (in_us * 1e-6) / 1e9,
+            "swap_out_per_block_memcpy_us": memcpy_us,
+            "swap_out_per_block_memcpy_gbs": moved / (memcpy_us * 1e-6) / 1e9,
+            "contiguous_d2h_memcpy_gbs": moved / (contiguous_us * 1e-6) / 1e9, "swap_pairs": n}
+
+
 def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     native.load()
@@ -497,6 +535,7 @@ def run_ours(args, rank, world, local_rank):
         rows["a7_copy_blocks_graph_gbs"] = ps_b / (copy_us * 1e-6) / 1e9
         rows["a7_copy_blocks_graph_pairs"] = int(ps.copy_pairs.shape[0])
         del ps, ck, cv
+        rows.update(swap_rows(w, stream))
 
     # ---- CPU oracle baseline (rank 0, one GPU only) ------------------------
     cpu = None
@@ -546,6 +585,87 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_beam(args, rank, world, local_rank):
+    """Beam search (64 requests x 4 beams, 1000-token prompts, 16-token
+    blocks, llama8b heads): every step forks and frees beams, copies shared
+    blocks (copy-on-write), writes one token per beam and decodes.  A timed
+    pass replays all steps of the trace; value = the steps' algorithmic bytes
+    / their time."""
+    torch.cuda.set_device(local_rank)
+    native.load()
+    t = workloads.beam_search(requests=64, beams=4, prompt_len=1000, steps=args.beam_steps, block_size=16,
+                              num_heads=32, num_kv_heads=8, head_dim=128, dtype=torch.bfloat16,
+                              seed=workloads.SEED_BASE + 10 + 1000 * rank, device="cuda")
+    stream = torch.cuda.current_stream()
+    k, v = t.k_cache, t.v_cache
+    elem = k.element_size()
+    part = args.partition_size or 512
+    max_ctx = max(int(st.context_lens.max()) for st in t.steps)
+    nseq = t.steps[0].context_lens.numel()
+    ws = torch.empty(api.decode_workspace_size(nseq, t.num_heads, max_ctx, part, t.head_dim), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty(nseq, t.num_heads, t.head_dim, device="cuda")
+    step_bytes, launches_per_pass, copies = 0, 0, 0
+    for st in t.steps:
+        n = int(st.copy_pairs.shape[0])
+        copies += n
+        step_bytes += metrics.decode_bytes(st.context_lens.tolist(), t.num_heads, t.num_kv_heads, t.head_dim, elem, 4)
+        step_bytes += metrics.write_bytes(nseq, t.num_kv_heads, t.head_dim, elem)
+        step_bytes += metrics.copy_bytes(n, 1, t.num_kv_heads, t.block_size, t.head_dim, elem)
+        launches_per_pass += (1 if n else 0) + 2 + (2 if int(st.context_lens.max()) > part else 0)
+
+    # Host-side facts of every step, taken before timing (no device sync in the loop).
+    plan = [(st, int(st.context_lens.max()), int(st.copy_pairs.shape[0])) for st in t.steps]
+
+    def one_pass():
+        for st, mc, n in plan:
+            if n:
+                api.copy_blocks([k], [v], st.copy_pairs)
+            api.reshape_and_cache(st.new_key, st.new_value, k, v, st.slot_mapping)
+            api.decode(st.query, k, v, st.block_tables, st.context_lens, t.scale, out=out,
+                       max_context_len=mc, partition_size=part, workspace=ws)
+
+    for _ in range(max(args.warmup // len(t.steps), 3)):
+        one_pass()
+    status, code = api.get_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error {status} ({code:#x}) during warm-up")
+    passes = max(1, args.steps // len(t.steps))
+    sampler = ClockSampler(local_rank)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)
+    s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(passes):
+        one_pass()
+    e0.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    status, code = api.get_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error {status} ({code:#x}) in the timed region")
+    nsteps = passes * len(t.steps)
+    step_ms = all_reduce_max(s0.elapsed_time(e0) / nsteps, world)
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    value = aggregate_throughput(world, step_bytes / len(t.steps), step_ms)
+    print(json.dumps({
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": nsteps, "warmup": args.warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"beam_search: 64 requests x 4 beams, 1000-token prompts, {len(t.steps)} steps, "
+                               f"d 128, 32/8 heads, bf16, block 16, partition {part}",
+                   "copy_on_write_pairs_per_step": copies / len(t.steps), "parallelism": f"replicas x{world}"},
+        "seq_decode_steps_per_s": world * nseq / (step_ms * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": value / world, "peak": float(peaks.get("hbm_gbs", 6800.0)),
+                     "unit": "GB/s", "frac": value / world / float(peaks.get("hbm_gbs", 6800.0)), "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "whole step (copy, write, decode)"},
+        "gpu_launches": passes * launches_per_pass, "clocks": clocks}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.decode_kernel == "simt":
@@ -564,7 +684,10 @@ def main():
         run_reference(args, rank, world)
         return
     try:
-        run_ours(args, rank, world, local_rank)
+        if args.workload == "beam_search":
+            run_beam(args, rank, world, local_rank)
+        else:
+            run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -12,6 +12,8 @@
  *        block-wise form; Review §3-2 "fused block read and attention")
  *   - pa_copy_blocks       : copy whole blocks for copy-on-write
  *       ("PagedAttention 论文精读笔记", §6.1; Review §3-2 "fused block copy")
+ *   - pa_swap_blocks       : move whole blocks between GPU and host memory
+ *       ("PagedAttention 论文精读笔记", §7.4)
  *
  * Conventions shared by every call
  *   - Pointers named "device" are CUDA device pointers of the current device;
@@ -61,7 +63,7 @@ typedef enum {
 #define PA_DEVERR_SLOT         0x2  /* slot_mapping entry >= num_blocks * block_size       */
 #define PA_DEVERR_CONTEXT_LEN  0x4  /* context_len < 0, > max_blocks_per_seq * block_size,
                                        or > the max_context_len the call was sized for    */
-#define PA_DEVERR_COPY_PAIR    0x8  /* copy pair id outside [0, num_blocks)                */
+#define PA_DEVERR_COPY_PAIR    0x8  /* copy or swap pair id outside its pool                */
 #define PA_DEVERR_TIMEOUT      0x10 /* a bounded wait inside a kernel ran out              */
 
 /* Shape of one layer's KV pool (K and V pools have the same shape). */
@@ -175,6 +177,31 @@ int pa_decode_noalloc(void *out, int32_t out_dtype, const void *query,
  */
 int pa_copy_blocks(void *const *k_caches, void *const *v_caches, int32_t num_layers,
                    const int64_t *src_dst_pairs, int64_t num_pairs,
+                   const pa_cache_desc *cache, void *stream);
+
+/*
+ * Swap blocks between two pools of the same block shape -- a GPU pool and a
+ * pool in page-locked host memory -- in one launch: swap-out (GPU -> host)
+ * when a sequence is preempted, swap-in (host -> GPU, possibly into other
+ * blocks) when it resumes ("PagedAttention 论文精读笔记", §7.4 swapping).  For
+ * every pair i and layer l, the K block src_k[l][pairs[i][0]] is copied to
+ * dst_k[l][pairs[i][1]], and the V block likewise.  The GPU reads and writes
+ * the host pool directly (unified addressing over the CPU-GPU link).
+ *   src_k, src_v, dst_k, dst_v  HOST arrays of num_layers pool pointers (1 <=
+ *                       num_layers <= 256); each pool is device memory,
+ *                       page-locked host memory (cudaHostAlloc / registered)
+ *                       or managed memory -- pageable host memory is
+ *                       PA_ERR_INVALID_ARG
+ *   src_num_blocks, dst_num_blocks  blocks in the source / destination pools
+ *   src_dst_pairs       int64 [num_pairs][2], device or page-locked host;
+ *                       destinations distinct
+ *   cache               block shape (num_kv_heads, block_size, head_dim, dtype);
+ *                       its num_blocks is not used
+ * A pair outside its pool sets PA_DEVERR_COPY_PAIR and is skipped.
+ */
+int pa_swap_blocks(void *const *src_k, void *const *src_v, int64_t src_num_blocks,
+                   void *const *dst_k, void *const *dst_v, int64_t dst_num_blocks,
+                   int32_t num_layers, const int64_t *src_dst_pairs, int64_t num_pairs,
                    const pa_cache_desc *cache, void *stream);
 
 /*

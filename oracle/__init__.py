@@ -61,12 +61,13 @@ class Oracle:
         lib.orc_elem_to_double.restype = dbl
         lib.orc_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i64, i64, i32, i32, i32, i32]
         lib.orc_copy_blocks.argtypes = [vp, vp, i32, vp, i64, i64, i64]
+        lib.orc_swap_blocks.argtypes = [vp, vp, i64, vp, vp, i64, i32, vp, i64, i64]
         lib.orc_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32,
                                    i32, i64, dbl, i32]
         lib.orc_decode_partitioned.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32,
                                                i32, i32, i64, dbl, i32]
         lib.orc_max_threads.argtypes = []
-        for name in ("orc_reshape_and_cache", "orc_copy_blocks", "orc_decode",
+        for name in ("orc_reshape_and_cache", "orc_copy_blocks", "orc_swap_blocks", "orc_decode",
                      "orc_decode_partitioned", "orc_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
         self.lib = lib
@@ -114,6 +115,17 @@ class Oracle:
         rc = self.lib.orc_copy_blocks(kp, vp, len(k_pools), self._ptr(pairs), pairs.shape[0], nb,
                                       block_bytes)
         self._check(rc, "copy_blocks")
+
+    def swap_blocks(self, src_k, src_v, dst_k, dst_v, pairs):
+        """In place on the destination pools: blocks pairs[i][0] of the
+        source pools to blocks pairs[i][1] of the destination pools."""
+        pairs = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+        n = len(src_k)
+        arr = lambda pools: (ctypes.c_void_p * n)(*[self._ptr(q) for q in pools])
+        rc = self.lib.orc_swap_blocks(arr(src_k), arr(src_v), src_k[0].shape[0], arr(dst_k), arr(dst_v),
+                                      dst_k[0].shape[0], n, self._ptr(pairs), pairs.shape[0],
+                                      src_k[0][0].nbytes)
+        self._check(rc, "swap_blocks")
 
     def decode(self, query, k_pool, v_pool, dtype, block_tables, context_lens, num_kv_heads,
                scale, num_threads=1, want_weight_sum=False):

@@ -135,6 +135,32 @@ int orc_copy_blocks(void *const *k_pools, void *const *v_pools, int num_layers,
 }
 
 /* ---------------------------------------------------------------------------
+ * Swapping.  "PagedAttention 论文精读笔记", §7.4: the blocks of an evicted
+ * sequence are copied to CPU memory, and back to (possibly different) GPU
+ * blocks when it is scheduled again.  Source and destination are two pools.
+ * ------------------------------------------------------------------------- */
+int orc_swap_blocks(void *const *src_k, void *const *src_v, int64_t src_num_blocks,
+                    void *const *dst_k, void *const *dst_v, int64_t dst_num_blocks,
+                    int num_layers, const int64_t *pairs, int64_t num_pairs, int64_t block_bytes)
+{
+    if (num_layers < 0 || num_pairs < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0 || block_bytes <= 0)
+        return ORC_EBADARG;
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        int64_t src = pairs[2 * i];
+        int64_t dst = pairs[2 * i + 1];
+        if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks)
+            return ORC_ERANGE;
+        for (int layer = 0; layer < num_layers; ++layer) {
+            memcpy((char *)dst_k[layer] + dst * block_bytes,
+                   (const char *)src_k[layer] + src * block_bytes, (size_t)block_bytes);
+            memcpy((char *)dst_v[layer] + dst * block_bytes,
+                   (const char *)src_v[layer] + src * block_bytes, (size_t)block_bytes);
+        }
+    }
+    return ORC_OK;
+}
+
+/* ---------------------------------------------------------------------------
  * Gather one sequence's logical K and V for one KV head into contiguous fp64
  * rows: row j (j < ctx) comes from physical block table[j / B], offset j % B.
  * ("PagedAttention 论文精读笔记", §4.2: K_j = (k_{(j-1)B+1} .. k_{jB}) is the

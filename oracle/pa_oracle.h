@@ -63,6 +63,15 @@ int orc_copy_blocks(void *const *k_pools, void *const *v_pools, int num_layers,
                     const int64_t *pairs, int64_t num_pairs, int64_t num_blocks,
                     int64_t block_bytes);
 
+/* Swap: for each pair in list order and each layer, copy the K block and the
+ * V block (block_bytes each) from block src of the source pools to block dst
+ * of the destination pools (a GPU pool and a host pool of the same block
+ * shape, in either direction).  "PagedAttention 论文精读笔记", §7.4: evicted
+ * blocks are copied to CPU memory and copied back when the sequence resumes. */
+int orc_swap_blocks(void *const *src_k, void *const *src_v, int64_t src_num_blocks,
+                    void *const *dst_k, void *const *dst_v, int64_t dst_num_blocks,
+                    int num_layers, const int64_t *pairs, int64_t num_pairs, int64_t block_bytes);
+
 /* Decode attention in fp64.  out is [num_seqs][num_heads][head_dim] doubles.
  * weight_sum (may be NULL) is [num_seqs][num_heads]: sum over attended tokens
  * of the normalised weights, which is 1 up to rounding (0 when ctx = 0).

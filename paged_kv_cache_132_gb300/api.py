@@ -126,6 +126,32 @@ def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tenso
                               _stream_ptr(stream)), "pa_copy_blocks")
 
 
+def swap_blocks(src_k: Sequence[torch.Tensor], src_v: Sequence[torch.Tensor], dst_k: Sequence[torch.Tensor],
+                dst_v: Sequence[torch.Tensor], src_dst_pairs: torch.Tensor,
+                stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy blocks pairs[i][0] of the source pools to blocks pairs[i][1] of
+    the destination pools, every layer, one launch: GPU <-> page-locked host
+    (swap-out / swap-in).  Host pools must be pinned (``pin_memory()``)."""
+    lib = native.load()
+    n = len(src_k)
+    _require(n > 0 and len(src_v) == n and len(dst_k) == n and len(dst_v) == n, "one pool per layer on each side")
+    pools = list(src_k) + list(src_v) + list(dst_k) + list(dst_v)
+    for p in pools:
+        _require(p.is_contiguous(), "pools must be contiguous")
+        _require(p.is_cuda or p.is_pinned(), "host pools must be in page-locked (pinned) memory")
+        _require(p.dtype == src_k[0].dtype and tuple(p.shape[1:]) == tuple(src_k[0].shape[1:]),
+                 "pools must share dtype and block shape")
+    _require(src_dst_pairs.dtype == torch.int64 and src_dst_pairs.dim() == 2 and src_dst_pairs.shape[1] == 2,
+             "src_dst_pairs is int64 [n][2]")
+    _require(src_dst_pairs.is_cuda or src_dst_pairs.is_pinned(), "pairs must be on the GPU or pinned")
+    _require(src_dst_pairs.is_contiguous(), "pairs must be contiguous")
+    desc = cache_desc(src_k[0])
+    arr = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])
+    _raise(lib.pa_swap_blocks(arr(src_k), arr(src_v), src_k[0].shape[0], arr(dst_k), arr(dst_v), dst_k[0].shape[0],
+                              n, src_dst_pairs.data_ptr(), src_dst_pairs.shape[0], ctypes.byref(desc),
+                              _stream_ptr(stream)), "pa_swap_blocks")
+
+
 def get_device_error(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:
     """(status, PA_DEVERR_* mask); synchronises the stream and clears the word."""
     code = ctypes.c_int32(0)

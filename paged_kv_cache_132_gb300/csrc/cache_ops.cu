@@ -7,10 +7,12 @@
 //    [NB][Hkv][B][d] in one pass, 16 bytes per thread, so that consecutive
 //    threads read consecutive bytes of the source and write whole rows of
 //    the destination.
-//  * copy_blocks: "fused block copy for copy-on-write" (same page, §3-2;
-//    "PagedAttention 论文精读笔记", §6.1).  One launch copies every (pair,
-//    layer, K|V) block, one CTA per block, each thread keeping several
-//    16-byte loads in flight before its stores.
+//  * block copies: "fused block copy for copy-on-write" (same page, §3-2;
+//    "PagedAttention 论文精读笔记", §6.1), and swapping between a GPU pool and
+//    a page-locked host pool (same notes, §7.4) -- the GPU reads and writes
+//    host memory directly through unified addressing, so one launch moves
+//    every (pair, layer, K|V) block instead of one memcpy per block.  One CTA
+//    per block, each thread keeping several 16-byte loads in flight.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -53,17 +55,21 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
     }
 }
 
-struct CopyPools {
-    uint4* k[kMaxCopyLayers];
-    uint4* v[kMaxCopyLayers];
+// Source and destination pools of a block copy: the same pools for
+// copy-on-write, a GPU pool and a page-locked host pool for swapping.
+struct BlockPools {
+    const uint4* src_k[kMaxCopyLayers];
+    const uint4* src_v[kMaxCopyLayers];
+    uint4* dst_k[kMaxCopyLayers];
+    uint4* dst_v[kMaxCopyLayers];
 };
 
 constexpr int kCopyThreads = 256;
 constexpr int kCopyUnroll = 8;
 
 __global__ void __launch_bounds__(kCopyThreads)
-copy_blocks_kernel(const __grid_constant__ CopyPools pools, int num_layers, const int64_t* __restrict__ pairs,
-                   int64_t num_blocks, int64_t vecs_per_block, int* err) {
+block_copy_kernel(const __grid_constant__ BlockPools pools, int num_layers, const int64_t* __restrict__ pairs,
+                  int64_t src_num_blocks, int64_t dst_num_blocks, int64_t vecs_per_block, int* err) {
     // blockIdx.x -> (pair, layer, K|V), K|V fastest.
     const int64_t id = blockIdx.x;
     const int is_value = (int)(id & 1);
@@ -71,13 +77,14 @@ copy_blocks_kernel(const __grid_constant__ CopyPools pools, int num_layers, cons
     const int64_t pair = (id >> 1) / num_layers;
     const int64_t src = __ldg(pairs + 2 * pair);
     const int64_t dst = __ldg(pairs + 2 * pair + 1);
-    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
         if (threadIdx.x == 0 && layer == 0 && !is_value) set_error(err, PA_DEVERR_COPY_PAIR);
         return;
     }
-    uint4* base = is_value ? pools.v[layer] : pools.k[layer];
-    const uint4* from = base + src * vecs_per_block;
-    uint4* to = base + dst * vecs_per_block;
+    const uint4* from = (is_value ? pools.src_v[layer] : pools.src_k[layer]) + src * vecs_per_block;
+    uint4* to = (is_value ? pools.dst_v[layer] : pools.dst_k[layer]) + dst * vecs_per_block;
+    // Several 16-byte loads in flight per thread before the stores (the
+    // source may be host memory, far away).
     for (int64_t i0 = threadIdx.x; i0 < vecs_per_block; i0 += (int64_t)kCopyThreads * kCopyUnroll) {
         uint4 buf[kCopyUnroll];
 #pragma unroll
@@ -91,6 +98,19 @@ copy_blocks_kernel(const __grid_constant__ CopyPools pools, int num_layers, cons
             if (i < vecs_per_block) to[i] = buf[u];
         }
     }
+}
+
+cudaError_t launch_block_copy(const BlockPools& pools, int num_layers, const int64_t* pairs, int64_t num_pairs,
+                              int64_t src_num_blocks, int64_t dst_num_blocks, const PoolShape& shape, int* err,
+                              cudaStream_t stream) {
+    if (num_pairs == 0) return cudaSuccess;
+    const int64_t block_bytes =
+        (int64_t)shape.num_kv_heads * shape.block_size * shape.head_dim * shape.elem_bytes;
+    const int64_t ctas = num_pairs * num_layers * 2;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    block_copy_kernel<<<(unsigned)ctas, kCopyThreads, 0, stream>>>(pools, num_layers, pairs, src_num_blocks,
+                                                                    dst_num_blocks, block_bytes / 16, err);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -113,19 +133,27 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
 cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
                                const int64_t* pairs, int64_t num_pairs, const PoolShape& shape,
                                int* err, cudaStream_t stream) {
-    if (num_pairs == 0) return cudaSuccess;
-    CopyPools pools{};
+    BlockPools pools{};
     for (int l = 0; l < num_layers; ++l) {
-        pools.k[l] = static_cast<uint4*>(k_caches[l]);
-        pools.v[l] = static_cast<uint4*>(v_caches[l]);
+        pools.src_k[l] = pools.dst_k[l] = static_cast<uint4*>(k_caches[l]);
+        pools.src_v[l] = pools.dst_v[l] = static_cast<uint4*>(v_caches[l]);
     }
-    const int64_t block_bytes =
-        (int64_t)shape.num_kv_heads * shape.block_size * shape.head_dim * shape.elem_bytes;
-    const int64_t ctas = num_pairs * num_layers * 2;
-    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-    copy_blocks_kernel<<<(unsigned)ctas, kCopyThreads, 0, stream>>>(pools, num_layers, pairs, shape.num_blocks,
-                                                                     block_bytes / 16, err);
-    return cudaGetLastError();
+    return launch_block_copy(pools, num_layers, pairs, num_pairs, shape.num_blocks, shape.num_blocks, shape, err,
+                             stream);
+}
+
+cudaError_t launch_swap_blocks(void* const* src_k, void* const* src_v, int64_t src_num_blocks, void* const* dst_k,
+                               void* const* dst_v, int64_t dst_num_blocks, int num_layers, const int64_t* pairs,
+                               int64_t num_pairs, const PoolShape& shape, int* err, cudaStream_t stream) {
+    BlockPools pools{};
+    for (int l = 0; l < num_layers; ++l) {
+        pools.src_k[l] = static_cast<const uint4*>(src_k[l]);
+        pools.src_v[l] = static_cast<const uint4*>(src_v[l]);
+        pools.dst_k[l] = static_cast<uint4*>(dst_k[l]);
+        pools.dst_v[l] = static_cast<uint4*>(dst_v[l]);
+    }
+    return launch_block_copy(pools, num_layers, pairs, num_pairs, src_num_blocks, dst_num_blocks, shape, err,
+                             stream);
 }
 
 }  // namespace pa

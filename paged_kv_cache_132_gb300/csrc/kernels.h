@@ -26,6 +26,9 @@ constexpr int kMaxCopyLayers = 256;
 cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
                                const int64_t* pairs, int64_t num_pairs, const PoolShape& shape,
                                int* err, cudaStream_t stream);
+cudaError_t launch_swap_blocks(void* const* src_k, void* const* src_v, int64_t src_num_blocks, void* const* dst_k,
+                               void* const* dst_v, int64_t dst_num_blocks, int num_layers, const int64_t* pairs,
+                               int64_t num_pairs, const PoolShape& shape, int* err, cudaStream_t stream);
 
 // ---- decode (decode_*.cu) ----------------------------------------------------
 // Everything one decode launch needs; passed by value as the kernel argument.

@@ -313,6 +313,46 @@ int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_lay
                                             static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+// Pool memory the GPU can address: device memory, page-locked host memory
+// or managed memory -- not pageable host memory.
+bool gpu_addressable(const void* p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // a failed query leaves no error behind for later calls
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeManaged;
+}
+}  // namespace
+
+int pa_swap_blocks(void* const* src_k, void* const* src_v, int64_t src_num_blocks, void* const* dst_k,
+                   void* const* dst_v, int64_t dst_num_blocks, int32_t num_layers, const int64_t* src_dst_pairs,
+                   int64_t num_pairs, const pa_cache_desc* cache, void* stream) {
+    pa::PoolShape shape;
+    int rc = check_cache(cache, &shape);
+    if (rc != PA_OK) return rc;
+    if (num_layers < 1 || num_layers > pa::kMaxCopyLayers || num_pairs < 0 || src_num_blocks <= 0 ||
+        dst_num_blocks <= 0 || !src_k || !src_v || !dst_k || !dst_v)
+        return PA_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PA_OK;
+    if (!aligned(src_dst_pairs, 8)) return PA_ERR_INVALID_ARG;
+    for (int l = 0; l < num_layers; ++l)
+        if (!aligned(src_k[l], 16) || !aligned(src_v[l], 16) || !aligned(dst_k[l], 16) || !aligned(dst_v[l], 16))
+            return PA_ERR_INVALID_ARG;
+    const int dev = current_device();
+    if (dev < 0) return PA_ERR_CUDA;
+    if (!gpu_addressable(src_dst_pairs)) return PA_ERR_INVALID_ARG;
+    for (int l = 0; l < num_layers; ++l)
+        if (!gpu_addressable(src_k[l]) || !gpu_addressable(src_v[l]) || !gpu_addressable(dst_k[l]) ||
+            !gpu_addressable(dst_v[l]))
+            return PA_ERR_INVALID_ARG;
+    int* err = error_word(dev);
+    if (!err) return PA_ERR_CUDA;
+    return status_of(pa::launch_swap_blocks(src_k, src_v, src_num_blocks, dst_k, dst_v, dst_num_blocks, num_layers,
+                                            src_dst_pairs, num_pairs, shape, err, static_cast<cudaStream_t>(stream)));
+}
+
 int pa_get_device_error(void* stream, int32_t* code) {
     if (!code) return PA_ERR_INVALID_ARG;
     *code = 0;

@@ -312,52 +312,64 @@ class BeamSearchTrace:
 
 def beam_search(*, beams: int = 4, prompt_len: int = 45, steps: int = 40, num_heads: int = 8,
                 num_kv_heads: int = 2, head_dim: int = 64, block_size: int = 4, dtype=torch.bfloat16,
-                seed: int = SEED_BASE + 10, device="cpu") -> BeamSearchTrace:
+                requests: int = 1, seed: int = SEED_BASE + 10, device="cpu") -> BeamSearchTrace:
     """A seeded beam-search trace ("PagedAttention 论文精读笔记", §6.2, Fig. 9).
 
-    The prompt is stored once and shared by all beams.  At every step each of
-    the `beams` new candidates picks a parent among the current beams
-    (uniformly, with replacement): parents picked several times are forked
-    (blocks shared, refcount + 1), beams not picked die and their blocks are
-    released (freed when the count reaches zero).  Every candidate then
-    appends its token; a shared last block is first copied (copy-on-write)."""
+    Each of `requests` prompts is stored once and shared by its beams.  At
+    every step each of a request's `beams` new candidates picks a parent among
+    that request's current beams (uniformly, with replacement): parents picked
+    several times are forked (blocks shared, refcount + 1), beams not picked
+    die and their blocks are released (freed when the count reaches zero).
+    Every candidate then appends its token; a shared last block is first
+    copied (copy-on-write).  Sequence r*beams + j is beam j of request r."""
     gen_cpu = torch.Generator().manual_seed(seed)
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     per_beam = blocks_needed(prompt_len + steps + 1, block_size)
-    num_blocks = blocks_needed(prompt_len, block_size) + beams * (per_beam + 2)
+    num_blocks = requests * (blocks_needed(prompt_len, block_size) + beams * (per_beam + 2))
     mgr = BlockManager(num_blocks, block_size, _permutation(num_blocks, gen_cpu))
-    mgr.add_sequence(0, prompt_len)
-    prompt_slots = mgr.prompt_slots(0)
-    keys = _normal((prompt_len, num_kv_heads, head_dim), dtype, gen, device)
-    values = _normal((prompt_len, num_kv_heads, head_dim), dtype, gen, device)
+    prompt_slots = []
+    live = []
+    next_id = 0
+    for _ in range(requests):
+        mgr.add_sequence(next_id, prompt_len)
+        prompt_slots.extend(mgr.prompt_slots(next_id))
+        live.append([next_id])
+        next_id += 1
+    n = len(prompt_slots)
+    keys = _normal((n, num_kv_heads, head_dim), dtype, gen, device)
+    values = _normal((n, num_kv_heads, head_dim), dtype, gen, device)
     k_cache = _pool_from_tokens(keys, prompt_slots, num_blocks, block_size)
     v_cache = _pool_from_tokens(values, prompt_slots, num_blocks, block_size)
-    live = [0]
-    next_id = 1
+    del keys, values
+    total = requests * beams
     out_steps = []
     for _ in range(steps):
         free_before = mgr.num_free()
-        parents = torch.randint(0, len(live), (beams,), generator=gen_cpu).tolist()
         new_live = []
-        for p in parents:
-            mgr.fork(live[p], next_id)
-            new_live.append(next_id)
-            next_id += 1
-        for seq in live:
-            mgr.free_sequence(seq)
+        for r in range(requests):
+            parents = torch.randint(0, len(live[r]), (beams,), generator=gen_cpu).tolist()
+            kids = []
+            for p in parents:
+                mgr.fork(live[r][p], next_id)
+                kids.append(next_id)
+                next_id += 1
+            for seq in live[r]:
+                mgr.free_sequence(seq)
+            new_live.append(kids)
         freed = mgr.num_free() - free_before
         live = new_live
-        slots = [mgr.append_token(seq) for seq in live]
+        seqs = [seq for kids in live for seq in kids]
+        slots = [mgr.append_token(seq) for seq in seqs]
         pairs = mgr.take_copies()
         out_steps.append(BeamStep(
             copy_pairs=torch.tensor(pairs, dtype=torch.int64, device=device).reshape(-1, 2),
             slot_mapping=torch.tensor(slots, dtype=torch.int64, device=device),
-            new_key=_normal((beams, num_kv_heads, head_dim), dtype, gen, device),
-            new_value=_normal((beams, num_kv_heads, head_dim), dtype, gen, device),
-            block_tables=_tables_tensor([mgr.table(seq) for seq in live]).to(device),
-            context_lens=torch.tensor([mgr.length(seq) for seq in live], dtype=torch.int32, device=device),
-            query=_normal((beams, num_heads, head_dim), dtype, gen, device),
+            new_key=_normal((total, num_kv_heads, head_dim), dtype, gen, device),
+            new_value=_normal((total, num_kv_heads, head_dim), dtype, gen, device),
+            block_tables=_tables_tensor([mgr.table(seq) for seq in seqs]).to(device),
+            context_lens=torch.tensor([mgr.length(seq) for seq in seqs], dtype=torch.int32, device=device),
+            query=_normal((total, num_heads, head_dim), dtype, gen, device),
             freed_blocks=freed))
     return BeamSearchTrace(num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
                            block_size=block_size, dtype=dtype, num_blocks=num_blocks,

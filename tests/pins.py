@@ -337,7 +337,35 @@ def check_copy_on_write(orc, golden):
                 assert np.array_equal(vps[layer][blk], before_v[layer][src])
 
 
+def check_swap_roundtrip(orc):
+    """Swap-out then swap-in restores the blocks; every moved block equals
+    numpy's fancy-indexed copy, every other block is untouched."""
+    rng = np.random.default_rng(5)
+    layers, gpu_nb, host_nb, shape = 2, 12, 7, (3, 4, 8)
+    gk = [rng.standard_normal((gpu_nb,) + shape).astype(np.float32) for _ in range(layers)]
+    gv = [rng.standard_normal((gpu_nb,) + shape).astype(np.float32) for _ in range(layers)]
+    hk = [np.zeros((host_nb,) + shape, np.float32) for _ in range(layers)]
+    hv = [np.zeros((host_nb,) + shape, np.float32) for _ in range(layers)]
+    out_pairs = np.array([[3, 0], [11, 4], [5, 6]], dtype=np.int64)
+    orc.swap_blocks(gk, gv, hk, hv, out_pairs)
+    for layer in range(layers):
+        assert np.array_equal(hk[layer][out_pairs[:, 1]], gk[layer][out_pairs[:, 0]])
+        assert np.array_equal(hv[layer][out_pairs[:, 1]], gv[layer][out_pairs[:, 0]])
+        untouched = np.setdiff1d(np.arange(host_nb), out_pairs[:, 1])
+        assert not hk[layer][untouched].any()
+    # back into different GPU blocks
+    back = np.array([[0, 7], [4, 8], [6, 9]], dtype=np.int64)
+    gk2 = [x.copy() for x in gk]
+    gv2 = [x.copy() for x in gv]
+    orc.swap_blocks(hk, hv, gk2, gv2, back)
+    for layer in range(layers):
+        assert np.array_equal(gk2[layer][[7, 8, 9]], gk[layer][[3, 11, 5]])
+        assert np.array_equal(gv2[layer][[7, 8, 9]], gv[layer][[3, 11, 5]])
+        keep = [b for b in range(gpu_nb) if b not in (7, 8, 9)]
+        assert np.array_equal(gk2[layer][keep], gk[layer][keep])
+
+
 ORACLE_CHECKS = [check_sdpa, check_weight_sums, check_block_permutation, check_stale_slots_ignored,
                  check_gqa_equals_repeated_mha, check_closed_forms, check_partition_merge,
-                 check_f16_decoding, check_bf16_decoding]
+                 check_f16_decoding, check_bf16_decoding, check_swap_roundtrip]
 GOLDEN_CHECKS = [check_walkthrough_write, check_figure6, check_address_lookup, check_copy_on_write]

@@ -111,3 +111,15 @@ def test_copy_blocks_rejects_on_host(lib):
 
 def test_get_device_error_needs_output(lib):
     assert lib.pa_get_device_error(None, None) == -1
+
+
+def test_swap_blocks_rejects_on_host(lib):
+    d = _desc()
+    ptrs = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    f = lib.pa_swap_blocks
+    assert f(ptrs, ptrs, 8, ptrs, ptrs, 8, 0, FAKE, 3, ctypes.byref(d), None) == -1      # no layers
+    assert f(ptrs, ptrs, 0, ptrs, ptrs, 8, 2, FAKE, 3, ctypes.byref(d), None) == -1      # empty source pool
+    assert f(ptrs, ptrs, 8, ptrs, ptrs, 8, 2, FAKE, 0, ctypes.byref(d), None) == 0       # nothing to move
+    assert f(ptrs, ptrs, 8, ptrs, ptrs, 8, 2, FAKE + 4, 3, ctypes.byref(d), None) == -1  # misaligned pairs
+    mis = (ctypes.c_void_p * 2)(FAKE, FAKE + 8)
+    assert f(ptrs, ptrs, 8, mis, ptrs, 8, 2, FAKE, 3, ctypes.byref(d), None) == -1

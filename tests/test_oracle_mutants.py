@@ -35,6 +35,8 @@ MUTANTS = {
     "copy_value_direction": ("memmove((char *)v_pools[layer] + dst * block_bytes,\n                    (const char *)v_pools[layer] + src * block_bytes, (size_t)block_bytes);",
                              "memmove((char *)v_pools[layer] + src * block_bytes,\n                    (const char *)v_pools[layer] + dst * block_bytes, (size_t)block_bytes);"),
     "merge_drops_rescale": ("L += l_p[p] * exp(m_p[p] - M);", "L += l_p[p];"),
+    "swap_value_from_key_pool": ("(const char *)src_v[layer] + src * block_bytes, (size_t)block_bytes);",
+                                 "(const char *)src_k[layer] + src * block_bytes, (size_t)block_bytes);"),
     "max_not_subtracted_in_weights": ("z[j] = exp(z[j] - M); /* z now holds the unnormalised weights w_j */",
                                       "z[j] = exp(z[j] - M) * (j == 0 ? 2.0 : 1.0);"),
 }
