@@ -66,9 +66,11 @@ class Oracle:
                                    i32, i64, dbl, i32]
         lib.orc_decode_partitioned.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32,
                                                i32, i32, i64, dbl, i32]
+        lib.orc_prefill.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i64, dbl,
+                                    i32]
         lib.orc_max_threads.argtypes = []
         for name in ("orc_reshape_and_cache", "orc_copy_blocks", "orc_swap_blocks", "orc_decode",
-                     "orc_decode_partitioned", "orc_max_threads"):
+                     "orc_decode_partitioned", "orc_prefill", "orc_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
         self.lib = lib
 
@@ -144,6 +146,23 @@ class Oracle:
                                  int(num_threads))
         self._check(rc, "decode")
         return (out, wsum) if want_weight_sum else out
+
+    def prefill(self, query, query_start, k_pool, v_pool, dtype, block_tables, context_lens, num_kv_heads, scale,
+                num_threads=1):
+        """fp64 prefill output [rows][H][d] for query rows [rows][H][d]."""
+        rows, h, d = query.shape
+        nb, hkv, bs, d2 = k_pool.shape
+        assert d2 == d and hkv == num_kv_heads
+        qs = np.ascontiguousarray(query_start, dtype=np.int32)
+        tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+        ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+        assert qs.size == ctx.size + 1 and qs[-1] == rows
+        out = np.zeros((rows, h, d), dtype=np.float64)
+        rc = self.lib.orc_prefill(self._ptr(out), self._ptr(query), self._ptr(qs), self._ptr(k_pool),
+                                  self._ptr(v_pool), dtype, self._ptr(tables), tables.shape[1], self._ptr(ctx),
+                                  ctx.size, h, hkv, bs, d, nb, float(scale), int(num_threads))
+        self._check(rc, "prefill")
+        return out
 
     def decode_partitioned(self, query, k_pool, v_pool, dtype, block_tables, context_lens,
                            num_kv_heads, scale, partition_size):

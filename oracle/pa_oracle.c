@@ -423,3 +423,79 @@ int orc_decode_partitioned(double *out,
     free(o_p);
     return status;
 }
+
+/* ---------------------------------------------------------------------------
+ * Prefill over a cached prefix: the same attention as orc_decode, for every
+ * new token of a sequence, each over the positions up to its own.
+ * ------------------------------------------------------------------------- */
+int orc_prefill(double *out, const void *query, const int32_t *query_start,
+                const void *k_pool, const void *v_pool, int dtype,
+                const int32_t *block_tables, int max_blocks_per_seq,
+                const int32_t *context_lens, int num_seqs,
+                int num_heads, int num_kv_heads, int block_size, int head_dim,
+                int64_t num_blocks, double scale, int num_threads)
+{
+    int rc = check_decode_args(context_lens, num_seqs, max_blocks_per_seq, num_heads,
+                               num_kv_heads, block_size, head_dim, num_blocks, dtype);
+    if (rc != ORC_OK)
+        return rc;
+    for (int s = 0; s < num_seqs; ++s) {
+        int n = query_start[s + 1] - query_start[s];
+        if (n < 0 || n > context_lens[s])
+            return ORC_EBADARG;
+    }
+    int group = num_heads / num_kv_heads;
+    int max_ctx = max_context(context_lens, num_seqs);
+    int64_t tasks = (int64_t)num_seqs * num_kv_heads;
+    int status = ORC_OK;
+#ifdef _OPENMP
+    if (num_threads <= 0)
+        num_threads = omp_get_max_threads();
+#else
+    num_threads = 1;
+#endif
+#pragma omp parallel num_threads(num_threads > 1 ? num_threads : 1)
+    {
+        size_t rows = (size_t)(max_ctx > 0 ? max_ctx : 1);
+        double *Kc = malloc(rows * head_dim * sizeof(double));
+        double *Vc = malloc(rows * head_dim * sizeof(double));
+        double *z = malloc(rows * sizeof(double));
+        double *q = malloc((size_t)head_dim * sizeof(double));
+        int local = (Kc && Vc && z && q) ? ORC_OK : ORC_ENOMEM;
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t task = 0; task < tasks; ++task) {
+            if (local != ORC_OK)
+                continue;
+            int s = (int)(task / num_kv_heads);
+            int kv_head = (int)(task % num_kv_heads);
+            int ctx = context_lens[s];
+            int first = query_start[s];
+            int n = query_start[s + 1] - first;
+            local = gather_sequence(Kc, Vc, k_pool, v_pool, dtype,
+                                    block_tables + (int64_t)s * max_blocks_per_seq, ctx, kv_head,
+                                    num_kv_heads, block_size, head_dim, num_blocks);
+            if (local != ORC_OK)
+                continue;
+            for (int i = 0; i < n; ++i) {
+                int position = ctx - n + i;
+                for (int g = 0; g < group; ++g) {
+                    int h = kv_head * group + g;
+                    int64_t row = (int64_t)(first + i) * num_heads + h;
+                    for (int k = 0; k < head_dim; ++k)
+                        q[k] = orc_elem_to_double(query, row * head_dim + k, dtype);
+                    attend(out + row * head_dim, NULL, NULL, NULL, q, Kc, Vc, position + 1, head_dim,
+                           scale, z);
+                }
+            }
+        }
+        if (local != ORC_OK) {
+#pragma omp critical
+            status = local;
+        }
+        free(Kc);
+        free(Vc);
+        free(z);
+        free(q);
+    }
+    return status;
+}

@@ -102,6 +102,21 @@ int orc_decode_partitioned(double *out,
                            int head_dim, int64_t num_blocks, double scale,
                            int partition_size);
 
+/* Prefill over a cached prefix ("PagedAttention 论文精读笔记", §6.3: with a
+ * shared prefix cached, the prompt phase computes only the user's part; §2.1
+ * attention equation).  Sequence s has n_s = query_start[s+1] - query_start[s]
+ * new tokens, the last n_s of its context_lens[s] cached tokens (their K/V are
+ * already in the pools).  Query row query_start[s] + i (i < n_s) sits at
+ * position p = context_lens[s] - n_s + i and attends to positions 0..p.
+ * out is [num_query_rows][num_heads][head_dim] doubles, num_query_rows =
+ * query_start[num_seqs]; query is [num_query_rows][num_heads][head_dim]. */
+int orc_prefill(double *out, const void *query, const int32_t *query_start,
+                const void *k_pool, const void *v_pool, int dtype,
+                const int32_t *block_tables, int max_blocks_per_seq,
+                const int32_t *context_lens, int num_seqs,
+                int num_heads, int num_kv_heads, int block_size, int head_dim,
+                int64_t num_blocks, double scale, int num_threads);
+
 /* Number of OpenMP threads the oracle would use for num_threads = 0 (all). */
 int orc_max_threads(void);
 

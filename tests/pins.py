@@ -365,7 +365,60 @@ def check_swap_roundtrip(orc):
         assert np.array_equal(gk2[layer][keep], gk[layer][keep])
 
 
+def _prefill_case(seed, lens, chunks, h, hkv, d, b, code):
+    """A paged case whose last chunks[i] tokens of sequence i are its new
+    (query) tokens; returns the case and the query rows [sum(chunks)][H][d]."""
+    case = paged_case(seed, lens, h, hkv, d, b, code)
+    g = torch.Generator().manual_seed(seed + 1)
+    q = torch.randn(sum(chunks), h, d, generator=g).to(TORCH_OF[code])
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    return case, q, qs
+
+
+def _run_prefill(orc, case, q, qs):
+    return orc.prefill(bits(q), qs, bits(case["k_pool"]), bits(case["v_pool"]), case["code"], case["tables"],
+                       np.array(case["lens"], dtype=np.int32), case["Hkv"], case["scale"])
+
+
+def check_prefill_vs_sdpa(orc):
+    """Every new token attends to the cached prefix and to the chunk up to
+    itself: torch float64 SDPA with that mask, on contiguous K/V."""
+    lens, chunks = [40, 7, 64, 33], [17, 7, 1, 32]
+    case, q, qs = _prefill_case(701, lens, chunks, 8, 2, 32, 8, O.BF16)
+    got = _run_prefill(orc, case, q, qs)
+    for i, (n, c) in enumerate(zip(lens, chunks)):
+        qi = q[qs[i]:qs[i + 1]].to(torch.float64).permute(1, 0, 2)[None]      # [1, H, c, d]
+        k = case["keys"][i].to(torch.float64).permute(1, 0, 2)[None]           # [1, Hkv, n, d]
+        v = case["values"][i].to(torch.float64).permute(1, 0, 2)[None]
+        pos = torch.arange(n - c, n)[:, None]
+        mask = torch.arange(n)[None, :] <= pos                                # [c, n]
+        ref = F.scaled_dot_product_attention(qi, k, v, attn_mask=mask, scale=case["scale"], enable_gqa=True)
+        err = float(np.max(np.abs(got[qs[i]:qs[i + 1]] - ref[0].permute(1, 0, 2).numpy())))
+        assert err <= 1e-12, f"prefill vs SDPA, sequence {i}: {err}"
+
+
+def check_prefill_special_cases(orc):
+    # (a) one new token per sequence is decode
+    lens = [5, 40, 17]
+    case, q, qs = _prefill_case(702, lens, [1, 1, 1], 4, 2, 16, 8, O.F16)
+    got = _run_prefill(orc, case, q, qs)
+    dec = orc.decode(bits(q), bits(case["k_pool"]), bits(case["v_pool"]), case["code"], case["tables"],
+                     np.array(lens, dtype=np.int32), case["Hkv"], case["scale"])
+    assert np.array_equal(got, dec), "a one-token chunk must equal decode"
+    # (b) no cached prefix: plain causal self-attention of the chunk
+    lens = [23, 9]
+    case, q, qs = _prefill_case(703, lens, lens, 4, 4, 16, 4, O.F32)
+    got = _run_prefill(orc, case, q, qs)
+    for i, n in enumerate(lens):
+        qi = q[qs[i]:qs[i + 1]].to(torch.float64).permute(1, 0, 2)[None]
+        k = case["keys"][i].to(torch.float64).permute(1, 0, 2)[None]
+        v = case["values"][i].to(torch.float64).permute(1, 0, 2)[None]
+        ref = F.scaled_dot_product_attention(qi, k, v, is_causal=True, scale=case["scale"])
+        assert np.max(np.abs(got[qs[i]:qs[i + 1]] - ref[0].permute(1, 0, 2).numpy())) <= 1e-12
+
+
 ORACLE_CHECKS = [check_sdpa, check_weight_sums, check_block_permutation, check_stale_slots_ignored,
                  check_gqa_equals_repeated_mha, check_closed_forms, check_partition_merge,
-                 check_f16_decoding, check_bf16_decoding, check_swap_roundtrip]
+                 check_f16_decoding, check_bf16_decoding, check_swap_roundtrip,
+                 check_prefill_vs_sdpa, check_prefill_special_cases]
 GOLDEN_CHECKS = [check_walkthrough_write, check_figure6, check_address_lookup, check_copy_on_write]

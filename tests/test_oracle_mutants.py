@@ -37,6 +37,9 @@ MUTANTS = {
     "merge_drops_rescale": ("L += l_p[p] * exp(m_p[p] - M);", "L += l_p[p];"),
     "swap_value_from_key_pool": ("(const char *)src_v[layer] + src * block_bytes, (size_t)block_bytes);",
                                  "(const char *)src_k[layer] + src * block_bytes, (size_t)block_bytes);"),
+    "prefill_position_off_by_one": ("int position = ctx - n + i;", "int position = ctx - n + i - 1;"),
+    "prefill_query_row": ("int64_t row = (int64_t)(first + i) * num_heads + h;",
+                          "int64_t row = (int64_t)(first + n - 1 - i) * num_heads + h;"),
     "max_not_subtracted_in_weights": ("z[j] = exp(z[j] - M); /* z now holds the unnormalised weights w_j */",
                                       "z[j] = exp(z[j] - M) * (j == 0 ? 2.0 : 1.0);"),
 }
