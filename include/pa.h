@@ -14,6 +14,9 @@
  *       ("PagedAttention 论文精读笔记", §6.1; Review §3-2 "fused block copy")
  *   - pa_swap_blocks       : move whole blocks between GPU and host memory
  *       ("PagedAttention 论文精读笔记", §7.4)
+ *   - pa_prefill           : prompt-phase attention of new tokens over a
+ *       cached prefix, causal within the new tokens
+ *       ("PagedAttention 论文精读笔记", §6.3 and §5.3)
  *
  * Conventions shared by every call
  *   - Pointers named "device" are CUDA device pointers of the current device;
@@ -163,6 +166,43 @@ int pa_decode_noalloc(void *out, int32_t out_dtype, const void *query,
                       const int32_t *context_lens, int32_t num_seqs, int32_t max_context_len,
                       int32_t num_heads, int32_t num_kv_heads, float scale, int32_t partition_size,
                       void *stream);
+
+/*
+ * Prefill over a cached prefix ("PagedAttention 论文精读笔记", §6.3: with a
+ * shared prefix held in cached physical blocks, the prompt phase computes
+ * only the request's own tokens; §2.1 attention equation; §5.3 prompt step).
+ * Sequence s has n_s = query_start_loc[s+1] - query_start_loc[s] new tokens,
+ * the LAST n_s of its context_lens[s] cached tokens: their K/V must already
+ * be in the pools (pa_reshape_and_cache earlier on the stream).  New token i
+ * of s sits at position context_lens[s] - n_s + i and attends to positions
+ * 0 .. context_lens[s] - n_s + i:
+ *   out[q][h][:] = sum_j softmax_j(scale * query[q][h] . k_j) v_j,
+ *   q = query_start_loc[s] + i, query head h reading KV head h / G,
+ *   G = num_heads / num_kv_heads.
+ *   out               device, [num_query_tokens][num_heads][head_dim] of
+ *                     out_dtype (any pa_dtype); rows not covered by a
+ *                     sequence are not written
+ *   query             device, [num_query_tokens][num_heads][head_dim] of
+ *                     cache->dtype
+ *   query_start_loc   device, int32 [num_seqs + 1], non-decreasing, last
+ *                     entry <= num_query_tokens
+ *   max_query_len     host, >= every n_s (sizes the launch)
+ *   block_tables      device, int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens      device, int32 [num_seqs], n_s <= context_lens[s] <=
+ *                     max_blocks_per_seq * block_size
+ * Computed on the tensor cores: P is rounded to the pools' 16-bit type
+ * before P.V; fp32 accumulation.  Supported: f16 or bf16 pools, G in
+ * {1, 2, 4, 8}, head_dim in {64, 128}, block_size in {8, 16, 32}; else
+ * PA_ERR_UNSUPPORTED.  A sequence whose lengths break the rules above sets
+ * PA_DEVERR_CONTEXT_LEN and is skipped; a bad block id sets
+ * PA_DEVERR_BLOCK_ID.  No workspace.
+ */
+int pa_prefill(void *out, int32_t out_dtype, const void *query, const int32_t *query_start_loc,
+               int32_t num_query_tokens, int32_t max_query_len,
+               const void *k_cache, const void *v_cache, const pa_cache_desc *cache,
+               const int32_t *block_tables, int32_t max_blocks_per_seq,
+               const int32_t *context_lens, int32_t num_seqs, int32_t num_heads,
+               int32_t num_kv_heads, float scale, void *stream);
 
 /*
  * Copy-on-write block copy, one launch for all pairs and layers.  For every

@@ -108,6 +108,41 @@ def decode(query: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
     return out
 
 
+def prefill(query: torch.Tensor, query_start_loc: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+            block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, max_query_len: int, *,
+            num_kv_heads: Optional[int] = None, out: Optional[torch.Tensor] = None,
+            out_dtype: torch.dtype = torch.float32, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Prompt-phase attention of new tokens over a cached prefix; returns
+    out [T][H][d].
+
+    Sequence s owns query rows query_start_loc[s] .. query_start_loc[s+1]-1,
+    the last n_s of its context_lens[s] cached tokens; row i attends to
+    positions 0 .. context_lens[s] - n_s + i.  ``max_query_len`` is a host-side
+    upper bound of every n_s."""
+    lib = native.load()
+    _check_cuda(query, query_start_loc, k_cache, v_cache, block_tables, context_lens)
+    _require(query.dim() == 3, "query is [num_tokens][num_heads][head_dim]")
+    t, h, d = query.shape
+    desc = cache_desc(k_cache)
+    _require(k_cache.shape == v_cache.shape and v_cache.dtype == k_cache.dtype, "K and V pools must match")
+    _require(query.dtype == k_cache.dtype and d == desc.head_dim, "query dtype/head_dim must match the pools")
+    _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2, "block_tables is int32 [S][max_blocks]")
+    s = block_tables.shape[0]
+    _require(context_lens.dtype == torch.int32 and context_lens.numel() == s, "context_lens is int32 [num_seqs]")
+    _require(query_start_loc.dtype == torch.int32 and query_start_loc.numel() == s + 1,
+             "query_start_loc is int32 [num_seqs + 1]")
+    hkv = desc.num_kv_heads if num_kv_heads is None else num_kv_heads
+    if out is None:
+        out = torch.empty((t, h, d), dtype=out_dtype, device=query.device)
+    _check_cuda(out)
+    _require(out.shape == (t, h, d) and out.dtype in DTYPE_CODE, "out is [num_tokens][num_heads][head_dim]")
+    _raise(lib.pa_prefill(out.data_ptr(), DTYPE_CODE[out.dtype], query.data_ptr(), query_start_loc.data_ptr(), t,
+                          int(max_query_len), k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(desc),
+                          block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(), s, h, hkv,
+                          float(scale), _stream_ptr(stream)), "pa_prefill")
+    return out
+
+
 def copy_blocks(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor], src_dst_pairs: torch.Tensor,
                 stream: Optional[torch.cuda.Stream] = None) -> None:
     """Copy-on-write: copy K and V block pairs[i][0] -> pairs[i][1] in every layer."""

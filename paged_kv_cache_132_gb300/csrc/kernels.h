@@ -102,4 +102,34 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype, int head_dim, int bl
                           int grid_items_upper_bound, DecodeVariant variant, const CUtensorMap* tmap_k,
                           const CUtensorMap* tmap_v, cudaStream_t stream);
 
+// ---- prefill over a cached prefix (prefill*.cu) -------------------------------
+struct PrefillParams {
+    void* out;
+    int out_dtype;
+    const int32_t* query_start;   // [num_seqs + 1] first query row of each sequence
+    const int32_t* block_tables;
+    int max_blocks;               // block table row length
+    const int32_t* context_lens;  // cached tokens, the new ones included
+    int num_seqs;
+    int num_tokens;               // rows of the query / output arrays
+    int max_query_len;            // upper bound of every sequence's new tokens
+    int num_heads;
+    int num_kv_heads;
+    int group_shift;              // log2(num_heads / num_kv_heads)
+    int block_size;
+    int64_t num_blocks;
+    int ctx_cap;                  // max_blocks * block_size
+    int tile_tokens;              // new tokens per CTA: 128 >> group_shift
+    int tiles_per_seq;            // ceil(max_query_len / tile_tokens)
+    float scale_log2;             // scale * log2(e)
+    int* err;
+    unsigned long long wait_limit_ns;
+};
+
+// tmap_q: the query [num_tokens][num_heads][d] as a 3-D tensor, box
+// {64, G, 128/G}; tmap_k / tmap_v: the pools as 2-D tensors [NB*Hkv*B][d],
+// box {64, B}; all with the 128-byte swizzle.  dtype PA_F16 or PA_BF16.
+cudaError_t launch_prefill(const PrefillParams& p, int dtype, int head_dim, const CUtensorMap* tmap_q,
+                           const CUtensorMap* tmap_k, const CUtensorMap* tmap_v, cudaStream_t stream);
+
 }  // namespace pa

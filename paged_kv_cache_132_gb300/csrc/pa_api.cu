@@ -118,7 +118,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // The pool [NB][Hkv][B][d] as a 2-D tensor of NB*Hkv*B rows of d 16-bit
 // elements; a box is 64 elements (128 bytes, the swizzle span) x B rows.
-bool encode_pool_map(CUtensorMap* map, const void* base, int dtype, const pa::PoolShape& shape) {
+// With interleave (the decode kernel, head_dim 128 and 8-token blocks) the
+// view is 3-D instead, one box per (block, head) tile.
+bool encode_pool_map(CUtensorMap* map, const void* base, int dtype, const pa::PoolShape& shape,
+                     bool interleave = true) {
     const int64_t rows = shape.num_blocks * shape.num_kv_heads * shape.block_size;
     if (rows <= 0 || rows >= (1LL << 31) || shape.head_dim % 64 != 0) return false;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
@@ -127,7 +130,7 @@ bool encode_pool_map(CUtensorMap* map, const void* base, int dtype, const pa::Po
         dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     std::memset(map, 0, sizeof(*map));
     CUresult r;
-    if (pa::interleaved_stage(shape.head_dim, shape.block_size)) {
+    if (interleave && pa::interleaved_stage(shape.head_dim, shape.block_size)) {
         // [rows][2 slabs][64]: one box = one whole (block, head) tile.
         const cuuint64_t dims[3] = {64, 2, (cuuint64_t)rows};
         const cuuint64_t strides[2] = {128, 256};
@@ -147,6 +150,25 @@ bool encode_pool_map(CUtensorMap* map, const void* base, int dtype, const pa::Po
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     return r == CUDA_SUCCESS;
+}
+
+// The query [num_tokens][num_heads][d] as a 3-D tensor {d, heads, tokens};
+// a box is 64 elements x the G heads of one KV head x 128/G tokens, i.e. the
+// 128 rows (token, grouped head) of one prefill tile, 128 bytes each.
+bool encode_query_map(CUtensorMap* map, const void* base, int dtype, int num_tokens, int num_heads, int head_dim,
+                      int group) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode || head_dim % 64 != 0) return false;
+    const CUtensorMapDataType type =
+        dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    std::memset(map, 0, sizeof(*map));
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads, (cuuint64_t)num_tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_heads * head_dim * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)(128 / group)};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    return encode(map, type, 3, const_cast<void*>(base), dims, strides, box, elem_strides,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Decode consumer: PA_DECODE_KERNEL=simt selects the CUDA-core kernels for
@@ -292,6 +314,66 @@ int pa_decode(void* out, int32_t out_dtype, const void* query, const void* k_cac
         variant = pa::kDecodeSimt;
     return status_of(pa::launch_decode(p, cache->dtype, shape.head_dim, shape.block_size, group, (int)items_ub,
                                        variant, &tmap_k, &tmap_v, static_cast<cudaStream_t>(stream)));
+}
+
+int pa_prefill(void* out, int32_t out_dtype, const void* query, const int32_t* query_start_loc,
+               int32_t num_query_tokens, int32_t max_query_len, const void* k_cache, const void* v_cache,
+               const pa_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+               const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, float scale,
+               void* stream) {
+    pa::PoolShape shape;
+    int rc = check_cache(cache, &shape);
+    if (rc != PA_OK) return rc;
+    if (elem_bytes(out_dtype) == 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs < 0 || num_query_tokens < 0 || max_query_len < 0 || num_heads <= 0 ||
+        num_kv_heads != cache->num_kv_heads || num_heads % num_kv_heads != 0 || max_blocks_per_seq <= 0 ||
+        !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || num_query_tokens == 0 || max_query_len == 0) return PA_OK;
+    if (!aligned(out, 16) || !aligned(query, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(query_start_loc, 4))
+        return PA_ERR_INVALID_ARG;
+    const int group = num_heads / num_kv_heads;
+    if (!(group == 1 || group == 2 || group == 4 || group == 8)) return PA_ERR_UNSUPPORTED;
+    if (cache->dtype == PA_F32) return PA_ERR_UNSUPPORTED;
+    if (!(shape.head_dim == 64 || shape.head_dim == 128)) return PA_ERR_UNSUPPORTED;
+    if (!(shape.block_size == 8 || shape.block_size == 16 || shape.block_size == 32)) return PA_ERR_UNSUPPORTED;
+
+    const int dev = current_device();
+    if (dev < 0) return PA_ERR_CUDA;
+    int* err = error_word(dev);
+    if (!err) return PA_ERR_CUDA;
+
+    pa::PrefillParams p{};
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.query_start = query_start_loc;
+    p.block_tables = block_tables;
+    p.max_blocks = max_blocks_per_seq;
+    p.context_lens = context_lens;
+    p.num_seqs = num_seqs;
+    p.num_tokens = num_query_tokens;
+    p.max_query_len = max_query_len;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group_shift = group == 1 ? 0 : group == 2 ? 1 : group == 4 ? 2 : 3;
+    p.block_size = shape.block_size;
+    p.num_blocks = shape.num_blocks;
+    const int64_t cap = (int64_t)max_blocks_per_seq * shape.block_size;
+    p.ctx_cap = (int)(cap < 0x7fffffffLL ? cap : 0x7fffffffLL);
+    p.tile_tokens = 128 / group;
+    p.tiles_per_seq = (max_query_len + p.tile_tokens - 1) / p.tile_tokens;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = err;
+    p.wait_limit_ns = wait_limit_ns();
+
+    CUtensorMap tmap_q, tmap_k, tmap_v;
+    if (!encode_query_map(&tmap_q, query, cache->dtype, num_query_tokens, num_heads, shape.head_dim, group) ||
+        !encode_pool_map(&tmap_k, k_cache, cache->dtype, shape, false) ||
+        !encode_pool_map(&tmap_v, v_cache, cache->dtype, shape, false))
+        return PA_ERR_UNSUPPORTED;
+    return status_of(pa::launch_prefill(p, cache->dtype, shape.head_dim, &tmap_q, &tmap_k, &tmap_v,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers, const int64_t* src_dst_pairs,

@@ -1,0 +1,11 @@
+// Prefill kernels for bf16 pools (head_dim 64 and 128).
+#include "prefill_launch.cuh"
+
+namespace pa {
+cudaError_t launch_prefill_bf16(const PrefillParams& p, int head_dim, const CUtensorMap* tq, const CUtensorMap* tk,
+                               const CUtensorMap* tv, cudaStream_t stream) {
+    if (head_dim == 64) return launch_prefill_t<__nv_bfloat16, 64>(p, tq, tk, tv, stream);
+    if (head_dim == 128) return launch_prefill_t<__nv_bfloat16, 128>(p, tq, tk, tv, stream);
+    return cudaErrorNotSupported;
+}
+}  // namespace pa

@@ -64,12 +64,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.pa_copy_blocks.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp, i64, desc, vp]
         lib.pa_swap_blocks.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i64, ctypes.POINTER(vp),
                                        ctypes.POINTER(vp), i64, i32, vp, i64, desc, vp]
+        lib.pa_prefill.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, desc, vp, i32, vp, i32, i32, i32,
+                                   ctypes.c_float, vp]
         lib.pa_get_device_error.argtypes = [vp, ctypes.POINTER(i32)]
         lib.pa_status_string.argtypes = [ctypes.c_int]
         lib.pa_status_string.restype = ctypes.c_char_p
         lib.pa_abi_version.argtypes = []
         for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_noalloc", "pa_copy_blocks",
-                     "pa_swap_blocks", "pa_get_device_error", "pa_abi_version"):
+                     "pa_swap_blocks", "pa_prefill", "pa_get_device_error", "pa_abi_version"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib

@@ -374,3 +374,149 @@ def beam_search(*, beams: int = 4, prompt_len: int = 45, steps: int = 40, num_he
     return BeamSearchTrace(num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
                            block_size=block_size, dtype=dtype, num_blocks=num_blocks,
                            scale=1.0 / math.sqrt(head_dim), k_cache=k_cache, v_cache=v_cache, steps=out_steps)
+
+
+# ---------------------------------------------------------------------------
+# prefill over a shared, cached prefix
+# ---------------------------------------------------------------------------
+@dataclass
+class PrefillStep:
+    """One prompt step over a cached prefix ("PagedAttention 论文精读笔记",
+    §6.3): copy-on-write of the shared partial last prefix block, then the new
+    tokens' K/V written to their slots, then attention of every new token over
+    the prefix and the new tokens up to itself."""
+    name: str
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    dtype: torch.dtype
+    num_blocks: int
+    scale: float
+    k_cache: torch.Tensor          # [NB][Hkv][B][d]: the prefixes cached, NaN elsewhere
+    v_cache: torch.Tensor
+    copy_pairs: torch.Tensor       # int64 [n][2]
+    new_key: torch.Tensor          # [T][Hkv][d], T = sum of the chunk lengths
+    new_value: torch.Tensor
+    slot_mapping: torch.Tensor     # int64 [T]
+    query: torch.Tensor            # [T][H][d]
+    query_start_loc: torch.Tensor  # int32 [S+1]
+    context_lens: torch.Tensor     # int32 [S]: prefix + chunk
+    block_tables: torch.Tensor     # int32 [S][max_blocks]
+    max_query_len: int
+    chunk_lens: List[int]
+    prefix_lens: List[int]
+    notes: Dict[str, object] = field(default_factory=dict)
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.chunk_lens)
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.query.shape[0])
+
+    def attended_pairs(self) -> int:
+        """(new token, position) pairs the step attends, per query head."""
+        return sum(n * p + n * (n + 1) // 2 for n, p in zip(self.chunk_lens, self.prefix_lens))
+
+
+PREFILL_WORKLOADS = ("prefill_tiny", "prefill_llama8b", "prefill_opt13b")
+
+
+def prefill_custom(chunk_lens: List[int], prefix_lens: List[int], *, prefix_groups: Optional[List[int]] = None,
+                   num_heads: int, num_kv_heads: int, head_dim: int, block_size: int, dtype: torch.dtype,
+                   seed: int = SEED_BASE + 20, device="cpu", name="prefill_custom",
+                   notes=None) -> PrefillStep:
+    """Requests with chunk_lens[s] new tokens after a cached prefix.
+    prefix_groups[s] names the prefix request s shares (default: its own);
+    prefix_lens[g] is the length of prefix g.  Each prefix is stored once
+    and forked into its requests (reference counts); a request's first new
+    token copies the shared partial last block (copy-on-write)."""
+    s_count = len(chunk_lens)
+    groups = list(range(s_count)) if prefix_groups is None else list(prefix_groups)
+    if len(groups) != s_count or any(g < 0 or g >= len(prefix_lens) for g in groups):
+        raise ValueError("prefix_groups must name one prefix per request")
+    gen_cpu = torch.Generator().manual_seed(seed)
+    holders = [10 ** 7 + g for g in range(len(prefix_lens))]
+
+    def simulate(num_blocks, free_order):
+        mgr = BlockManager(num_blocks, block_size, free_order)
+        hist = []
+        for g, plen in enumerate(prefix_lens):
+            mgr.add_sequence(holders[g], plen)
+            hist.extend(mgr.prompt_slots(holders[g]))
+        for s in range(s_count):
+            mgr.fork(holders[groups[s]], s)
+        new = []
+        for s in range(s_count):
+            for _ in range(chunk_lens[s]):
+                new.append(mgr.append_token(s))
+        return mgr, hist, new, num_blocks - mgr.num_free()
+
+    bound = sum(blocks_needed(p, block_size) for p in prefix_lens) + sum(
+        blocks_needed(prefix_lens[groups[s]] + chunk_lens[s], block_size) + 1 for s in range(s_count))
+    _, _, _, used = simulate(max(bound, 1), None)
+    nb = max(math.ceil(1.1 * used), 1)
+    mgr, hist, new, _ = simulate(nb, _permutation(nb, gen_cpu))
+    pairs = mgr.take_copies()
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    keys = _normal((len(hist), num_kv_heads, head_dim), dtype, gen, device)
+    values = _normal((len(hist), num_kv_heads, head_dim), dtype, gen, device)
+    k_cache = _pool_from_tokens(keys, hist, nb, block_size)
+    v_cache = _pool_from_tokens(values, hist, nb, block_size)
+    del keys, values
+    t = len(new)
+    starts = [0]
+    for n in chunk_lens:
+        starts.append(starts[-1] + n)
+    per_seq_prefix = [prefix_lens[groups[s]] for s in range(s_count)]
+    return PrefillStep(
+        name=name, num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=block_size,
+        dtype=dtype, num_blocks=nb, scale=1.0 / math.sqrt(head_dim), k_cache=k_cache, v_cache=v_cache,
+        copy_pairs=torch.tensor(pairs, dtype=torch.int64, device=device).reshape(-1, 2),
+        new_key=_normal((t, num_kv_heads, head_dim), dtype, gen, device),
+        new_value=_normal((t, num_kv_heads, head_dim), dtype, gen, device),
+        slot_mapping=torch.tensor(new, dtype=torch.int64, device=device),
+        query=_normal((t, num_heads, head_dim), dtype, gen, device),
+        query_start_loc=torch.tensor(starts, dtype=torch.int32, device=device),
+        context_lens=torch.tensor([per_seq_prefix[s] + chunk_lens[s] for s in range(s_count)], dtype=torch.int32,
+                                  device=device),
+        block_tables=_tables_tensor([mgr.table(s) for s in range(s_count)]).to(device),
+        max_query_len=max(chunk_lens + [0]), chunk_lens=list(chunk_lens), prefix_lens=per_seq_prefix,
+        notes=dict(notes or {}, unique_blocks_used=used))
+
+
+def make_prefill(name: str, device="cpu", *, num_seqs: Optional[int] = None,
+                 seed: Optional[int] = None) -> PrefillStep:
+    """The prefill workloads (stand-ins for the pages' shared-prefix
+    translation workload, with a synthetic few-shot prefix; no dataset):
+
+      prefill_tiny     3 requests, chunks {1, 50, 130} after one shared 37-token
+                       prefix, 8 query / 2 KV heads, d 64, bf16, B 16.
+      prefill_llama8b  32 requests sharing one 1024-token prefix, chunks
+                       ~ U[128, 1024]; 32 query / 8 KV heads, d 128, bf16, B 16.
+      prefill_opt13b   16 requests, 4 prefixes of 512 tokens (4 requests each),
+                       chunks ~ U[128, 1024]; 40 heads (MHA), d 128, f16, B 16.
+    """
+    if name not in PREFILL_WORKLOADS:
+        raise KeyError(f"unknown prefill workload {name!r}; choose from {PREFILL_WORKLOADS}")
+    seed = SEED_BASE + 30 + PREFILL_WORKLOADS.index(name) if seed is None else seed
+    gen_cpu = torch.Generator().manual_seed(seed)
+    if name == "prefill_tiny":
+        chunks = [1, 50, 130][: num_seqs or 3]
+        return prefill_custom(chunks, [37], prefix_groups=[0] * len(chunks), num_heads=8, num_kv_heads=2,
+                              head_dim=64, block_size=16, dtype=torch.bfloat16, seed=seed, device=device,
+                              name=name)
+    if name == "prefill_llama8b":
+        s = num_seqs or 32
+        chunks = torch.randint(128, 1025, (32,), generator=gen_cpu).tolist()[:s]
+        return prefill_custom(chunks, [1024], prefix_groups=[0] * s, num_heads=32, num_kv_heads=8, head_dim=128,
+                              block_size=16, dtype=torch.bfloat16, seed=seed, device=device, name=name,
+                              notes={"chunks": "U[128,1024]", "prefix": 1024})
+    s = num_seqs or 16
+    chunks = torch.randint(128, 1025, (16,), generator=gen_cpu).tolist()[:s]
+    return prefill_custom(chunks, [512] * 4, prefix_groups=[i % 4 for i in range(s)], num_heads=40,
+                          num_kv_heads=40, head_dim=128, block_size=16, dtype=torch.float16, seed=seed,
+                          device=device, name=name, notes={"chunks": "U[128,1024]", "prefix": "4 x 512"})

@@ -123,3 +123,40 @@ def test_swap_blocks_rejects_on_host(lib):
     assert f(ptrs, ptrs, 8, ptrs, ptrs, 8, 2, FAKE + 4, 3, ctypes.byref(d), None) == -1  # misaligned pairs
     mis = (ctypes.c_void_p * 2)(FAKE, FAKE + 8)
     assert f(ptrs, ptrs, 8, mis, ptrs, 8, 2, FAKE, 3, ctypes.byref(d), None) == -1
+
+
+def _prefill(lib, **over):
+    a = dict(out=FAKE, out_dtype=native.PA_F32, query=FAKE, qsl=FAKE, tokens=40, max_q=20, k=FAKE, v=FAKE,
+             desc=_desc(), tables=FAKE, max_blocks=4, ctx=FAKE, num_seqs=2, num_heads=4, num_kv_heads=2,
+             scale=0.125, stream=None)
+    a.update(over)
+    return lib.pa_prefill(a["out"], a["out_dtype"], a["query"], a["qsl"], a["tokens"], a["max_q"], a["k"], a["v"],
+                          ctypes.byref(a["desc"]), a["tables"], a["max_blocks"], a["ctx"], a["num_seqs"],
+                          a["num_heads"], a["num_kv_heads"], a["scale"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(desc=_desc(nb=0)), -1),
+    (dict(out_dtype=9), -1),
+    (dict(num_kv_heads=3), -1),
+    (dict(num_heads=5), -1),                    # not a multiple of num_kv_heads
+    (dict(tokens=-1), -1),
+    (dict(max_q=-2), -1),
+    (dict(max_blocks=0), -1),
+    (dict(scale=float("inf")), -1),
+    (dict(query=FAKE + 8), -1),                 # misaligned
+    (dict(qsl=FAKE + 2), -1),
+    (dict(out=0), -1),
+    (dict(desc=_desc(dtype=native.PA_F32)), -2),  # tensor cores: 16-bit pools only
+    (dict(num_heads=32, num_kv_heads=2), -2),   # group 16
+    (dict(desc=_desc(d=96)), -2),
+    (dict(desc=_desc(bs=4)), -2),
+])
+def test_prefill_rejects_on_host(lib, over, status):
+    assert _prefill(lib, **over) == status
+
+
+def test_prefill_nothing_to_do_is_noop(lib):
+    assert _prefill(lib, num_seqs=0) == 0
+    assert _prefill(lib, tokens=0) == 0
+    assert _prefill(lib, max_q=0) == 0
