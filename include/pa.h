@@ -190,8 +190,9 @@ int pa_decode_noalloc(void *out, int32_t out_dtype, const void *query,
  *   block_tables      device, int32 [num_seqs][max_blocks_per_seq]
  *   context_lens      device, int32 [num_seqs], n_s <= context_lens[s] <=
  *                     max_blocks_per_seq * block_size
- * Computed on the tensor cores: P is rounded to the pools' 16-bit type
- * before P.V; fp32 accumulation.  Supported: f16 or bf16 pools, G in
+ * scale must be > 0.  Computed on the tensor cores with fp32 accumulation;
+ * the weights P enter P.V as the pools' 16-bit type (bf16: as the sum of two
+ * bf16 halves).  Supported: f16 or bf16 pools, G in
  * {1, 2, 4, 8}, head_dim in {64, 128}, block_size in {8, 16, 32}; else
  * PA_ERR_UNSUPPORTED.  A sequence whose lengths break the rules above sets
  * PA_DEVERR_CONTEXT_LEN and is skipped; a bad block id sets

@@ -327,7 +327,7 @@ int pa_prefill(void* out, int32_t out_dtype, const void* query, const int32_t* q
     if (elem_bytes(out_dtype) == 0) return PA_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_query_tokens < 0 || max_query_len < 0 || num_heads <= 0 ||
         num_kv_heads != cache->num_kv_heads || num_heads % num_kv_heads != 0 || max_blocks_per_seq <= 0 ||
-        !std::isfinite(scale))
+        !std::isfinite(scale) || !(scale > 0.f))
         return PA_ERR_INVALID_ARG;
     if (num_seqs == 0 || num_query_tokens == 0 || max_query_len == 0) return PA_OK;
     if (!aligned(out, 16) || !aligned(query, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||

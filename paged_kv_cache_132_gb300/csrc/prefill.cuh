@@ -12,21 +12,31 @@
 // One CTA computes a tile of 128 query rows of one (sequence, KV head): the
 // rows are (token, grouped query head) pairs, 128/G tokens x G heads, so the
 // G query heads that share a KV head share every K/V tile (GQA).  The keys
-// and values are streamed in tiles of 128 positions.  Per tile j:
-//   S_j = Q K_j^T          tcgen05.mma, M=128 N=128 K=d, into TMEM (2 buffers)
-//   P_j = 2^(S_j*c - m)    softmax warps, one thread per row, P to shared
-//                          memory as 16-bit K-major rows
-//   O  += P_j V_j          tcgen05.mma, M=128 N=d K=128, O in TMEM
+// and values are streamed in tiles of 64 positions.  Per tile j:
+//   S_j = Q K_j^T          tcgen05.mma, M=128 N=64 K=d, into TMEM (2 buffers)
+//   P_j = 2^(S_j*c - m)    softmax warps, one thread per row; P is written
+//                          over S_j in TMEM as 16-bit values
+//   O  += P_j V_j          tcgen05.mma with A = P read from TMEM,
+//                          M=128 N=d K=64, O in TMEM
 // with the running max m kept in base-2 units (c = scale * log2 e) and O
 // rescaled only when a row's max grows by more than 8 (a factor of 256).
+// For bf16 pools P = P_hi + P_lo (two bf16 halves, two P.V products), which
+// keeps the output error near 2^-14 relative instead of the 2^-9 of one
+// bf16 rounding; f16 keeps one rounding (2^-11).
 //
-// Warp roles (192 threads, one CTA per SM):
-//   warps 0-3 softmax: thread r owns row r = TMEM lane r; mask, exponentials,
-//             row sums, P, the rare rescale of O, and at the end O / sum;
+// Two CTAs share an SM (each ~97 KiB of shared memory and 256 TMEM columns):
+// while one waits on its chain S_j -> softmax_j -> P_j V_j, the other's
+// MMAs keep the tensor cores busy, and one CTA's set-up and epilogue overlap
+// the other's work.
+//
+// Warp roles (192 threads):
+//   warps 0-3 softmax: thread r owns row r = TMEM lane r: mask,
+//             exponentials, row sums, P, the rare rescale of O, and at the
+//             end O / sum;
 //   warp 4    producer: Q once (3-D tensor copy: 128/G tokens x G heads x
 //             64-element slabs), then K and V tiles through the block table,
 //             one 2-D tensor copy per (block, 64-element slab), into a
-//             2-stage ring;
+//             stage ring;
 //   warp 5    MMA issuer (one thread) and owner of the TMEM allocation.
 // The MMA thread issues S_{j+1} before P_j.V_j, so the tensor cores compute
 // the next scores while the softmax warps work on the current ones.
@@ -47,16 +57,18 @@ namespace pa {
 
 template <int D>
 struct PrefillShape {
-    static constexpr int BM = 128;          // query rows per CTA
-    static constexpr int BN = 128;          // key/value positions per tile
-    static constexpr int SLABS = D / 64;    // 64-element (128-byte) column slabs of a row
-    static constexpr int SLAB = 128 * 128;  // bytes of one slab of 128 rows
-    static constexpr int NSTAGE = 3;
+    static constexpr int BM = 128;                 // query rows per CTA
+    static constexpr int BN = 64;                  // key/value positions per tile
+    static constexpr int SLABS = D / 64;           // 64-element (128-byte) column slabs of a row
+    static constexpr int Q_SLAB = BM * 128;        // bytes of one Q slab
+    static constexpr int KV_SLAB = BN * 128;       // bytes of one K or V slab
+    static constexpr int NSTAGE = D == 128 ? 2 : 4;
     static constexpr int SOFTMAX_WARPS = 4;
     static constexpr int PRODUCER_WARP = 4;
     static constexpr int MMA_WARP = 5;
     static constexpr int THREADS = 6 * 32;
-    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int CTAS_PER_SM = 2;
+    static constexpr uint32_t TMEM_COLS = 256;     // half of an SM's: two CTAs
     // TMEM columns: S buffer b at b*BN; its P (16-bit, two per column) is
     // written over it: P (or P_hi) in the first BN/2 columns, P_lo in the
     // next BN/2.  The output accumulator O after the two buffers.
@@ -65,25 +77,25 @@ struct PrefillShape {
     static_assert(O_COL + D <= TMEM_COLS, "TMEM columns");
 
     struct Smem {
-        alignas(1024) uint8_t q[SLABS][SLAB];
-        alignas(1024) uint8_t k[NSTAGE][SLABS][SLAB];
-        alignas(1024) uint8_t v[NSTAGE][SLABS][SLAB];
+        alignas(1024) uint8_t q[SLABS][Q_SLAB];
+        alignas(1024) uint8_t k[NSTAGE][SLABS][KV_SLAB];
+        alignas(1024) uint8_t v[NSTAGE][SLABS][KV_SLAB];
         uint64_t q_full;
         uint64_t k_full[NSTAGE];
         uint64_t v_full[NSTAGE];
-        uint64_t kv_empty[NSTAGE];
+        uint64_t k_empty[NSTAGE];  // S_j complete: K slot free (MMA commit)
+        uint64_t v_empty[NSTAGE];  // P_j V_j complete: V slot free (MMA commit)
         uint64_t s_full[2];    // S_j in buffer j % 2 (MMA commit)
         uint64_t p_full[2];    // P_j written over it (softmax warps)
-        uint64_t pv_done[2];   // P_j V_j complete: buffer j % 2 and O free again
+        uint64_t pv_done[2];   // P_j V_j complete: buffer j % 2 free again
         uint64_t mma_done;
         uint32_t tmem_base;
         int abort_flag;
     };
-    // At least 120 KiB, so that no two CTAs share an SM: the 512-column TMEM
-    // allocation then never has to wait for another CTA.
-    static constexpr int SMEM_BYTES =
-        (int)sizeof(Smem) + 1024 > 120 * 1024 ? (int)sizeof(Smem) + 1024 : 120 * 1024;
-    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
+    static constexpr int SMEM_BYTES = (int)sizeof(Smem) + 1024;
+    // Two CTAs per SM, and never three: the two 256-column TMEM allocations
+    // then never wait for one another.
+    static_assert(SMEM_BYTES <= 113 * 1024 && 3 * (SMEM_BYTES + 1024) > 228 * 1024, "two CTAs per SM");
 };
 
 // Tensor copies without an L2 hint: a K/V tile is read again by the other
@@ -102,6 +114,20 @@ __device__ inline void tma_load_3d_plain(void* dst, const CUtensorMap* map, int 
         "%4}], [%5];" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
         : "memory");
+}
+
+// Non-blocking test of an mbarrier phase (the MMA issuer polls two
+// conditions and must not sleep on either).
+__device__ inline bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
 }
 
 template <class Smem>
@@ -130,63 +156,77 @@ __device__ void prefill_producer(const PrefillParams& p, typename Shape::Smem& s
     const int BS = p.block_size;
     const uint32_t box_bytes = (uint32_t)BS * 128u;
     const int32_t* trow = p.block_tables + (int64_t)w.seq * p.max_blocks;
+    const uint64_t lim = p.wait_limit_ns;
     if (lane == 0) {
-        mbar_arrive_expect_tx(&sm.q_full, Shape::SLABS * Shape::SLAB);
+        mbar_arrive_expect_tx(&sm.q_full, Shape::SLABS * Shape::Q_SLAB);
 #pragma unroll
         for (int slab = 0; slab < Shape::SLABS; ++slab)
             tma_load_3d_plain(sm.q[slab], tq, slab * 64, w.kv_head << p.group_shift, w.qrow0, &sm.q_full);
     }
-    uint32_t filled = 0, parity = 0;  // per stage: filled at least once / parity of its last fill
+    // Blocks of tile jj: lane l holds the physical block of its l-th block
+    // (l < blocks of the tile), -1 elsewhere.  Loaded two tiles ahead.
+    auto blocks_of = [&](int jj) -> int {
+        if (jj >= w.nt) return -1;
+        const int kv0 = jj * Shape::BN;
+        const int nblk = (min(Shape::BN, w.kv_end - kv0) + BS - 1) / BS;  // <= 8: block_size >= 8
+        return lane < nblk ? __ldg(trow + kv0 / BS + lane) : -2;
+    };
+    int e0 = blocks_of(0), e1 = blocks_of(1);
+    uint32_t kfill = 0, kpar = 0, vfill = 0, vpar = 0;  // per slot: filled / parity of the last fill
     bool ok_run = true;
     for (int j = 0; j < w.nt; ++j) {
+        const int e2 = blocks_of(j + 2);
         const int st = j % Shape::NSTAGE;
         const uint32_t ph = (uint32_t)(j / Shape::NSTAGE) & 1u;
+        const int phys = e0;
+        const bool needed = phys != -2 && lane * BS < Shape::BN;
+        const bool ok = needed && phys >= 0 && (int64_t)phys < p.num_blocks;
+        if (needed && !ok && lane * BS < w.kv_end - j * Shape::BN) set_error(p.err, PA_DEVERR_BLOCK_ID);
+        const uint32_t bytes = (uint32_t)__popc(__ballot_sync(kFullMask, ok)) * Shape::SLABS * box_bytes;
+        const int y = ok ? (int)(((int64_t)phys * p.num_kv_heads + w.kv_head) * BS) : 0;
+        // K_j once S_{j-NSTAGE} has completed
         bool free_ok = true;
-        if (lane == 0) free_ok = mbar_wait_bounded(&sm.kv_empty[st], ph ^ 1u, p.wait_limit_ns);
-        free_ok = __shfl_sync(kFullMask, free_ok, 0);
-        if (!free_ok) {
+        if (lane == 0) free_ok = mbar_wait_bounded(&sm.k_empty[st], ph ^ 1u, lim);
+        if (!__shfl_sync(kFullMask, free_ok, 0)) {
             ok_run = false;
             break;
         }
-        if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) break;
-        const int kv0 = j * Shape::BN;
-        const int ntok = min(Shape::BN, w.kv_end - kv0);
-        const int nblk = (ntok + BS - 1) / BS;  // <= 16: block_size >= 8
-        int phys = -1;
-        bool ok = false;
-        if (lane < nblk) {
-            phys = __ldg(trow + kv0 / BS + lane);
-            ok = phys >= 0 && (int64_t)phys < p.num_blocks;
-            if (!ok) set_error(p.err, PA_DEVERR_BLOCK_ID);
-        }
-        const uint32_t bytes = (uint32_t)__popc(__ballot_sync(kFullMask, ok)) * Shape::SLABS * box_bytes;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&sm.k_full[st], bytes);
-            mbar_arrive_expect_tx(&sm.v_full[st], bytes);
-        }
+        if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[st], bytes);
         __syncwarp();
         if (ok) {
-            const int y = (int)(((int64_t)phys * p.num_kv_heads + w.kv_head) * BS);
 #pragma unroll
             for (int slab = 0; slab < Shape::SLABS; ++slab)
                 tma_load_2d_plain(sm.k[st][slab] + lane * box_bytes, tk, slab * 64, y, &sm.k_full[st]);
+        }
+        kfill |= 1u << st;
+        kpar = (kpar & ~(1u << st)) | (ph << st);
+        // V_j once P_{j-NSTAGE} V_{j-NSTAGE} has completed
+        if (lane == 0) free_ok = mbar_wait_bounded(&sm.v_empty[st], ph ^ 1u, lim);
+        if (!__shfl_sync(kFullMask, free_ok, 0)) {
+            ok_run = false;
+            break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[st], bytes);
+        __syncwarp();
+        if (ok) {
 #pragma unroll
             for (int slab = 0; slab < Shape::SLABS; ++slab)
                 tma_load_2d_plain(sm.v[st][slab] + lane * box_bytes, tv, slab * 64, y, &sm.v_full[st]);
         }
-        filled |= 1u << st;
-        parity = (parity & ~(1u << st)) | (ph << st);
+        vfill |= 1u << st;
+        vpar = (vpar & ~(1u << st)) | (ph << st);
+        if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) break;
+        e0 = e1;
+        e1 = e2;
     }
     if (!ok_run && lane == 0) prefill_abort(p, sm);
     pdl_launch_dependents();
     // Every copy this warp issued lands before the CTA exits (bounded).
     if (lane == 0) {
-        bool drained = mbar_wait_bounded(&sm.q_full, 0, p.wait_limit_ns);
+        bool drained = mbar_wait_bounded(&sm.q_full, 0, lim);
         for (int st = 0; st < Shape::NSTAGE; ++st) {
-            if (!(filled & (1u << st))) continue;
-            const uint32_t ph = (parity >> st) & 1u;
-            drained = mbar_wait_bounded(&sm.k_full[st], ph, p.wait_limit_ns) && drained;
-            drained = mbar_wait_bounded(&sm.v_full[st], ph, p.wait_limit_ns) && drained;
+            if (kfill & (1u << st)) drained = mbar_wait_bounded(&sm.k_full[st], (kpar >> st) & 1u, lim) && drained;
+            if (vfill & (1u << st)) drained = mbar_wait_bounded(&sm.v_full[st], (vpar >> st) & 1u, lim) && drained;
         }
         if (!drained) set_error(p.err, PA_DEVERR_TIMEOUT);
     }
@@ -203,51 +243,70 @@ __device__ void prefill_mma(const PrefillParams& p, typename Shape::Smem& sm, ui
     const uint64_t lim = p.wait_limit_ns;
     const uint32_t q_base = smem_addr(sm.q[0]);
 
-    // O += P_jj V_jj: A = P from TMEM (8 columns per 16 positions), B = V
-    // MN-major (head_dim along N, slabs Shape::SLAB bytes apart).  With
+    // S_js = Q K_js^T into buffer js % 2; the K slot is released when it completes.
+    auto issue_s = [&](int js) {
+        const int b = js & 1, st = js % Shape::NSTAGE;
+        const uint32_t k_base = smem_addr(sm.k[st][0]);
+#pragma unroll
+        for (int ks = 0; ks < KS_S; ++ks)
+            mma_f16_ss(tmem + b * Shape::BN,
+                       smem_desc_sw128(q_base + (ks >> 2) * Shape::Q_SLAB + (ks & 3) * 32, 16, 1024),
+                       smem_desc_sw128(k_base + (ks >> 2) * Shape::KV_SLAB + (ks & 3) * 32, 16, 1024), IDESC_S,
+                       ks > 0 ? 1u : 0u);
+        mma_commit(&sm.s_full[b]);
+        mma_commit(&sm.k_empty[st]);
+    };
+    // O += P_jp V_jp: A = P from TMEM (8 columns per 16 positions), B = V
+    // MN-major (head_dim along N, slabs Shape::KV_SLAB bytes apart).  With
     // SPLIT_P the 16-bit P is P_hi + P_lo and both halves are multiplied.
-    auto issue_pv = [&](int jj) -> bool {
-        const int b = jj & 1, st = jj % Shape::NSTAGE;
-        if (!mbar_wait_bounded(&sm.p_full[b], (uint32_t)(jj >> 1) & 1u, lim)) return false;
-        if (!mbar_wait_bounded(&sm.v_full[st], (uint32_t)(jj / Shape::NSTAGE) & 1u, lim)) return false;
-        tc_fence_after_sync();
+    auto issue_pv = [&](int jp) {
+        const int b = jp & 1, st = jp % Shape::NSTAGE;
         const uint32_t v_base = smem_addr(sm.v[st][0]);
         const uint32_t p_tmem = tmem + b * Shape::BN;
 #pragma unroll
         for (int ks = 0; ks < KS_O; ++ks)
             mma_f16_ts(tmem + Shape::O_COL, p_tmem + ks * 8,
-                       smem_desc_sw128(v_base + ks * 16 * 128, Shape::SLAB, 1024), IDESC_O,
-                       (jj > 0 || ks > 0) ? 1u : 0u);
+                       smem_desc_sw128(v_base + ks * 16 * 128, Shape::KV_SLAB, 1024), IDESC_O,
+                       (jp > 0 || ks > 0) ? 1u : 0u);
         if constexpr (SPLIT_P) {
 #pragma unroll
             for (int ks = 0; ks < KS_O; ++ks)
                 mma_f16_ts(tmem + Shape::O_COL, p_tmem + Shape::BN / 2 + ks * 8,
-                           smem_desc_sw128(v_base + ks * 16 * 128, Shape::SLAB, 1024), IDESC_O, 1u);
+                           smem_desc_sw128(v_base + ks * 16 * 128, Shape::KV_SLAB, 1024), IDESC_O, 1u);
         }
         mma_commit(&sm.pv_done[b]);
-        mma_commit(&sm.kv_empty[st]);
-        return true;
+        mma_commit(&sm.v_empty[st]);
     };
 
+    // Issue, in order within each kind, whichever is ready first: S_js (its
+    // K landed and buffer js % 2 is free: P_{js-2} V_{js-2} complete) or
+    // P_jp V_jp (P written, V landed).  At most two S ahead of the P.V.
     bool ok = mbar_wait_bounded(&sm.q_full, 0, lim);
-    for (int j = 0; ok && j < nt; ++j) {
-        const int b = j & 1, st = j % Shape::NSTAGE;
-        // K_j landed, and buffer b is free (P_{j-2} V_{j-2} complete).
-        ok = mbar_wait_bounded(&sm.k_full[st], (uint32_t)(j / Shape::NSTAGE) & 1u, lim) &&
-             mbar_wait_bounded(&sm.pv_done[b], ((uint32_t)(j >> 1) & 1u) ^ 1u, lim);
-        if (!ok) break;
-        tc_fence_after_sync();
-        const uint32_t k_base = smem_addr(sm.k[st][0]);
-#pragma unroll
-        for (int ks = 0; ks < KS_S; ++ks) {
-            const uint32_t off = (ks >> 2) * Shape::SLAB + (ks & 3) * 32;
-            mma_f16_ss(tmem + b * Shape::BN, smem_desc_sw128(q_base + off, 16, 1024),
-                       smem_desc_sw128(k_base + off, 16, 1024), IDESC_S, ks > 0 ? 1u : 0u);
+    int js = 0, jp = 0;
+    uint64_t idle_since = 0;
+    while (ok && jp < nt) {
+        bool did = false;
+        if (js < nt && js < jp + 2 &&
+            mbar_test(&sm.k_full[js % Shape::NSTAGE], (uint32_t)(js / Shape::NSTAGE) & 1u) &&
+            mbar_test(&sm.pv_done[js & 1], ((uint32_t)(js >> 1) & 1u) ^ 1u)) {
+            tc_fence_after_sync();
+            issue_s(js++);
+            did = true;
         }
-        mma_commit(&sm.s_full[b]);
-        if (j >= 1) ok = issue_pv(j - 1);
+        if (jp < js && mbar_test(&sm.p_full[jp & 1], (uint32_t)(jp >> 1) & 1u) &&
+            mbar_test(&sm.v_full[jp % Shape::NSTAGE], (uint32_t)(jp / Shape::NSTAGE) & 1u)) {
+            tc_fence_after_sync();
+            issue_pv(jp++);
+            did = true;
+        }
+        if (did) {
+            idle_since = 0;
+        } else {
+            const uint64_t now = global_timer_ns();
+            if (idle_since == 0) idle_since = now;
+            else if (now - idle_since > lim) ok = false;
+        }
     }
-    if (ok) ok = issue_pv(nt - 1);
     if (!ok) prefill_abort(p, sm);
     // Nothing this thread issued may still be running when TMEM is released.
     mma_commit(&sm.mma_done);
@@ -293,7 +352,7 @@ __device__ void prefill_softmax(const PrefillParams& p, typename Shape::Smem& sm
     // Rows past the chunk's end compute something finite and are not stored.
     const int last = valid ? w.ctx - w.n + i : w.kv_end - 1;
     const uint32_t row_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    const float c = p.scale_log2;
+    const float c = p.scale_log2;  // > 0
     float m = NEG_INF, l = 0.f;
     bool ok = true;
 
@@ -303,36 +362,29 @@ __device__ void prefill_softmax(const PrefillParams& p, typename Shape::Smem& sm
         if (!ok) break;
         tc_fence_after_sync();
         float x[BN];
+        {
+            uint32_t u[BN];
+            tmem_ld_x64(row_addr + b * BN, u);
 #pragma unroll
-        for (int h = 0; h < BN / 64; ++h) {
-            uint32_t u[64];
-            tmem_ld_x64(row_addr + b * BN + h * 64, u);
-#pragma unroll
-            for (int k = 0; k < 64; ++k) x[h * 64 + k] = __uint_as_float(u[k]);
+            for (int k = 0; k < BN; ++k) x[k] = __uint_as_float(u[k]);
         }
 
-        // Scores in base-2 units; positions after `last` get -inf.  Eight
-        // independent partial maxima / sums keep the dependency chains short.
+        // Raw-score maximum (positions after `last` are -inf), with eight
+        // independent partial maxima.
         const int kv0 = j * BN;
+        if (kv0 + BN - 1 > last) {
+#pragma unroll
+            for (int k = 0; k < BN; ++k) x[k] = kv0 + k <= last ? x[k] : NEG_INF;
+        }
         float pm[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) pm[q] = NEG_INF;
-        if (kv0 + BN - 1 <= last) {
+        for (int q = 0; q < 8; ++q) pm[q] = x[q];
 #pragma unroll
-            for (int k = 0; k < BN; ++k) {
-                x[k] *= c;
-                pm[k & 7] = fmaxf(pm[k & 7], x[k]);
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < BN; ++k) {
-                x[k] = kv0 + k <= last ? x[k] * c : NEG_INF;
-                pm[k & 7] = fmaxf(pm[k & 7], x[k]);
-            }
-        }
-        const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-        const float m_new = fmaxf(m, mx);
+        for (int k = 8; k < BN; ++k) pm[k & 7] = fmaxf(pm[k & 7], x[k]);
+        const float mx =
+            fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+        // Reference max in base-2 units.
+        const float m_new = fmaxf(m, mx * c);
         const bool grow = m_new > m + 8.f;  // always on the first tile (m = -inf)
         float alpha = 1.f;
         if (grow) {
@@ -340,52 +392,56 @@ __device__ void prefill_softmax(const PrefillParams& p, typename Shape::Smem& sm
             m = m_new;
             l *= alpha;
         }
+        const float nm = -m;
         float ps[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) ps[q] = 0.f;
 #pragma unroll
         for (int k = 0; k < BN; ++k) {
-            x[k] = exp2_approx(x[k] - m);
+            x[k] = exp2_approx(fmaf(x[k], c, nm));
             ps[k & 7] += x[k];
         }
         l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
 
-        // P over S in TMEM.  bf16: P = P_hi + P_lo, both truncated to 16
-        // bits (relative error below 2^-14); f16: P rounded once (2^-11).
+        // P over S in TMEM.  bf16: P = P_hi + P_lo, both truncated to 16 bits
+        // (relative error below 2^-14); f16: P rounded once (2^-11).
         {
-            uint32_t u[64];
+            uint32_t u[BN / 2];
             if constexpr (SPLIT_P) {
 #pragma unroll
-                for (int k = 0; k < 64; ++k) u[k] = pack_hi_halves(x[2 * k], x[2 * k + 1]);
-                tmem_st_x64(row_addr + b * BN, u);
+                for (int k = 0; k < BN / 2; ++k) u[k] = pack_hi_halves(x[2 * k], x[2 * k + 1]);
+                tmem_st_x32(row_addr + b * BN, u);
 #pragma unroll
-                for (int k = 0; k < 64; ++k) {
+                for (int k = 0; k < BN / 2; ++k) {
                     const float a = x[2 * k] - __uint_as_float(__float_as_uint(x[2 * k]) & 0xffff0000u);
                     const float e = x[2 * k + 1] - __uint_as_float(__float_as_uint(x[2 * k + 1]) & 0xffff0000u);
                     u[k] = pack_hi_halves(a, e);
                 }
-                tmem_st_x64(row_addr + b * BN + BN / 2, u);
+                tmem_st_x32(row_addr + b * BN + BN / 2, u);
             } else {
 #pragma unroll
-                for (int k = 0; k < 64; ++k) u[k] = pack_rn<T>(x[2 * k], x[2 * k + 1]);
-                tmem_st_x64(row_addr + b * BN, u);
+                for (int k = 0; k < BN / 2; ++k) u[k] = pack_rn<T>(x[2 * k], x[2 * k + 1]);
+                tmem_st_x32(row_addr + b * BN, u);
             }
         }
 
         // Value rows past kv_end (slots after the context, blocks not loaded)
         // may hold anything, NaN included; their weight is 0 but 0 * NaN is
-        // NaN, so the last tile's rows there are zeroed.
-        if (j == w.nt - 1 && w.kv_end - kv0 < BN) {
+        // NaN, so the last tile's rows there are zeroed: row r & 63, half of
+        // its 16-byte chunks (by r / 64) in swizzled order.
+        const int vrow0 = w.kv_end - kv0;
+        if (j == w.nt - 1 && vrow0 < BN) {
             const int st = j % Shape::NSTAGE;
             ok = __all_sync(kFullMask,
                             mbar_wait_bounded(&sm.v_full[st], (uint32_t)(j / Shape::NSTAGE) & 1u, lim));
             if (!ok) break;
-            if (r >= w.kv_end - kv0) {
+            const int vr = r & (BN - 1), vh = r / BN;
+            if (vr >= vrow0) {
 #pragma unroll
                 for (int slab = 0; slab < Shape::SLABS; ++slab) {
-                    uint4* row = reinterpret_cast<uint4*>(sm.v[st][slab] + r * 128);
+                    uint4* row = reinterpret_cast<uint4*>(sm.v[st][slab] + vr * 128);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) row[k] = make_uint4(0u, 0u, 0u, 0u);
+                    for (int k = 0; k < 4; ++k) row[(vh * 4 + k) ^ (vr & 7)] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             fence_proxy_async_smem();
@@ -436,7 +492,7 @@ __device__ void prefill_softmax(const PrefillParams& p, typename Shape::Smem& sm
 // the kernel: one CTA per (query tile, sequence, KV head)
 // ---------------------------------------------------------------------------
 template <typename T, int D>
-__global__ void __launch_bounds__(PrefillShape<D>::THREADS, 1)
+__global__ void __launch_bounds__(PrefillShape<D>::THREADS, PrefillShape<D>::CTAS_PER_SM)
     prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v) {
     using Shape = PrefillShape<D>;
@@ -478,7 +534,8 @@ __global__ void __launch_bounds__(PrefillShape<D>::THREADS, 1)
         for (int st = 0; st < Shape::NSTAGE; ++st) {
             mbar_init(&sm.k_full[st], 1);
             mbar_init(&sm.v_full[st], 1);
-            mbar_init(&sm.kv_empty[st], 1);
+            mbar_init(&sm.k_empty[st], 1);
+            mbar_init(&sm.v_empty[st], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.s_full[b], 1);

@@ -155,4 +155,25 @@ __device__ inline void tmem_st_x64(uint32_t taddr, const uint32_t (&r)[64]) {
         : "memory");
 }
 
+// One 32-bit column of this thread's TMEM lane: load (waited for) / store
+// (completed before returning).
+__device__ inline uint32_t tmem_ld_x1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r)
+        : "r"(taddr)
+        : "memory");
+    return r;
+}
+
+__device__ inline void tmem_st_x1(uint32_t taddr, uint32_t v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(v)
+        : "memory");
+}
+
 }  // namespace pa

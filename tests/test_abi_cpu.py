@@ -144,6 +144,8 @@ def _prefill(lib, **over):
     (dict(max_q=-2), -1),
     (dict(max_blocks=0), -1),
     (dict(scale=float("inf")), -1),
+    (dict(scale=0.0), -1),
+    (dict(scale=-0.125), -1),
     (dict(query=FAKE + 8), -1),                 # misaligned
     (dict(qsl=FAKE + 2), -1),
     (dict(out=0), -1),
