@@ -29,15 +29,17 @@
 // MMAs keep the tensor cores busy, and one CTA's set-up and epilogue overlap
 // the other's work.
 //
-// Warp roles (192 threads):
+// Warp roles (224 threads):
 //   warps 0-3 softmax: thread r owns row r = TMEM lane r: mask,
 //             exponentials, row sums, P, the rare rescale of O, and at the
 //             end O / sum;
-//   warp 4    producer: Q once (3-D tensor copy: 128/G tokens x G heads x
-//             64-element slabs), then K and V tiles through the block table,
-//             one 2-D tensor copy per (block, 64-element slab), into a
-//             stage ring;
-//   warp 5    MMA issuer (one thread) and owner of the TMEM allocation.
+//   warp 4    producer of Q (once; 3-D tensor copy: 128/G tokens x G heads
+//             x 64-element slabs) and of the K tiles, through the block
+//             table, one 2-D tensor copy per (block, 64-element slab), into
+//             a ring of slots released as soon as S_j has completed;
+//   warp 5    producer of the V tiles, likewise (slots released when
+//             P_j V_j has completed);
+//   warp 6    MMA issuer (one thread) and owner of the TMEM allocation.
 // The MMA thread issues S_{j+1} before P_j.V_j, so the tensor cores compute
 // the next scores while the softmax warps work on the current ones.
 // Every wait is bounded; a wait that runs out sets PA_DEVERR_TIMEOUT, the
@@ -64,9 +66,10 @@ struct PrefillShape {
     static constexpr int KV_SLAB = BN * 128;       // bytes of one K or V slab
     static constexpr int NSTAGE = D == 128 ? 2 : 4;
     static constexpr int SOFTMAX_WARPS = 4;
-    static constexpr int PRODUCER_WARP = 4;
-    static constexpr int MMA_WARP = 5;
-    static constexpr int THREADS = 6 * 32;
+    static constexpr int K_WARP = 4;    // Q and the K tiles
+    static constexpr int V_WARP = 5;    // the V tiles
+    static constexpr int MMA_WARP = 6;
+    static constexpr int THREADS = 7 * 32;
     static constexpr int CTAS_PER_SM = 2;
     static constexpr uint32_t TMEM_COLS = 256;     // half of an SM's: two CTAs
     // TMEM columns: S buffer b at b*BN; its P (16-bit, two per column) is
@@ -150,84 +153,78 @@ struct PrefillTile {
 // ---------------------------------------------------------------------------
 // producer warp
 // ---------------------------------------------------------------------------
-template <class Shape>
+// One producer warp streams either the K tiles (and Q first) or the V tiles
+// of the CTA's positions into its ring; slot st of tile j is refilled once
+// the MMA that read tile j - NSTAGE from it has completed (empty[st]).
+template <class Shape, bool IS_K>
 __device__ void prefill_producer(const PrefillParams& p, typename Shape::Smem& sm, int lane, const PrefillTile& w,
-                                 const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv) {
+                                 const CUtensorMap* tq, const CUtensorMap* tkv) {
     const int BS = p.block_size;
     const uint32_t box_bytes = (uint32_t)BS * 128u;
     const int32_t* trow = p.block_tables + (int64_t)w.seq * p.max_blocks;
     const uint64_t lim = p.wait_limit_ns;
-    if (lane == 0) {
+    uint64_t* full = IS_K ? sm.k_full : sm.v_full;
+    uint64_t* empty = IS_K ? sm.k_empty : sm.v_empty;
+    if (IS_K && lane == 0) {
         mbar_arrive_expect_tx(&sm.q_full, Shape::SLABS * Shape::Q_SLAB);
 #pragma unroll
         for (int slab = 0; slab < Shape::SLABS; ++slab)
             tma_load_3d_plain(sm.q[slab], tq, slab * 64, w.kv_head << p.group_shift, w.qrow0, &sm.q_full);
     }
-    // Blocks of tile jj: lane l holds the physical block of its l-th block
-    // (l < blocks of the tile), -1 elsewhere.  Loaded two tiles ahead.
+    // Blocks of tile jj: lane l < (blocks of the tile) holds its l-th
+    // physical block, other lanes -2.  Each entry is loaded two tiles before
+    // its use (the loop body runs twice per iteration so that no copy of a
+    // register still in flight is needed).
     auto blocks_of = [&](int jj) -> int {
-        if (jj >= w.nt) return -1;
+        if (jj >= w.nt) return -2;
         const int kv0 = jj * Shape::BN;
         const int nblk = (min(Shape::BN, w.kv_end - kv0) + BS - 1) / BS;  // <= 8: block_size >= 8
         return lane < nblk ? __ldg(trow + kv0 / BS + lane) : -2;
     };
-    int e0 = blocks_of(0), e1 = blocks_of(1);
-    uint32_t kfill = 0, kpar = 0, vfill = 0, vpar = 0;  // per slot: filled / parity of the last fill
+    uint32_t fill = 0, par = 0;  // per slot: filled / parity of its last fill
     bool ok_run = true;
-    for (int j = 0; j < w.nt; ++j) {
-        const int e2 = blocks_of(j + 2);
-        const int st = j % Shape::NSTAGE;
-        const uint32_t ph = (uint32_t)(j / Shape::NSTAGE) & 1u;
-        const int phys = e0;
-        const bool needed = phys != -2 && lane * BS < Shape::BN;
-        const bool ok = needed && phys >= 0 && (int64_t)phys < p.num_blocks;
-        if (needed && !ok && lane * BS < w.kv_end - j * Shape::BN) set_error(p.err, PA_DEVERR_BLOCK_ID);
-        const uint32_t bytes = (uint32_t)__popc(__ballot_sync(kFullMask, ok)) * Shape::SLABS * box_bytes;
-        const int y = ok ? (int)(((int64_t)phys * p.num_kv_heads + w.kv_head) * BS) : 0;
-        // K_j once S_{j-NSTAGE} has completed
-        bool free_ok = true;
-        if (lane == 0) free_ok = mbar_wait_bounded(&sm.k_empty[st], ph ^ 1u, lim);
-        if (!__shfl_sync(kFullMask, free_ok, 0)) {
-            ok_run = false;
-            break;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[st], bytes);
-        __syncwarp();
-        if (ok) {
+    int ea = blocks_of(0), eb = blocks_of(1);
+    for (int j = 0; j < w.nt; j += 2) {
 #pragma unroll
-            for (int slab = 0; slab < Shape::SLABS; ++slab)
-                tma_load_2d_plain(sm.k[st][slab] + lane * box_bytes, tk, slab * 64, y, &sm.k_full[st]);
-        }
-        kfill |= 1u << st;
-        kpar = (kpar & ~(1u << st)) | (ph << st);
-        // V_j once P_{j-NSTAGE} V_{j-NSTAGE} has completed
-        if (lane == 0) free_ok = mbar_wait_bounded(&sm.v_empty[st], ph ^ 1u, lim);
-        if (!__shfl_sync(kFullMask, free_ok, 0)) {
-            ok_run = false;
-            break;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[st], bytes);
-        __syncwarp();
-        if (ok) {
+        for (int h = 0; h < 2; ++h) {
+            const int jj = j + h;
+            if (jj >= w.nt) break;
+            const int phys = h == 0 ? ea : eb;
+            const int st = jj % Shape::NSTAGE;
+            const uint32_t ph = (uint32_t)(jj / Shape::NSTAGE) & 1u;
+            const bool needed = phys != -2;
+            const bool ok = needed && phys >= 0 && (int64_t)phys < p.num_blocks;
+            if (IS_K && needed && !ok) set_error(p.err, PA_DEVERR_BLOCK_ID);
+            const uint32_t bytes = (uint32_t)__popc(__ballot_sync(kFullMask, ok)) * Shape::SLABS * box_bytes;
+            bool free_ok = true;
+            if (lane == 0) free_ok = mbar_wait_bounded(&empty[st], ph ^ 1u, lim);
+            if (!__shfl_sync(kFullMask, free_ok, 0)) {
+                ok_run = false;
+                break;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
+            __syncwarp();
+            if (ok) {
+                const int y = (int)(((int64_t)phys * p.num_kv_heads + w.kv_head) * BS);
+                uint8_t* dst = IS_K ? sm.k[st][0] : sm.v[st][0];
 #pragma unroll
-            for (int slab = 0; slab < Shape::SLABS; ++slab)
-                tma_load_2d_plain(sm.v[st][slab] + lane * box_bytes, tv, slab * 64, y, &sm.v_full[st]);
+                for (int slab = 0; slab < Shape::SLABS; ++slab)
+                    tma_load_2d_plain(dst + slab * Shape::KV_SLAB + lane * box_bytes, tkv, slab * 64, y, &full[st]);
+            }
+            fill |= 1u << st;
+            par = (par & ~(1u << st)) | (ph << st);
+            if (h == 0) ea = blocks_of(jj + 2);
+            else eb = blocks_of(jj + 2);
         }
-        vfill |= 1u << st;
-        vpar = (vpar & ~(1u << st)) | (ph << st);
-        if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) break;
-        e0 = e1;
-        e1 = e2;
+        if (!ok_run || *reinterpret_cast<volatile int*>(&sm.abort_flag)) break;
     }
     if (!ok_run && lane == 0) prefill_abort(p, sm);
-    pdl_launch_dependents();
+    if (IS_K) pdl_launch_dependents();
     // Every copy this warp issued lands before the CTA exits (bounded).
     if (lane == 0) {
-        bool drained = mbar_wait_bounded(&sm.q_full, 0, lim);
-        for (int st = 0; st < Shape::NSTAGE; ++st) {
-            if (kfill & (1u << st)) drained = mbar_wait_bounded(&sm.k_full[st], (kpar >> st) & 1u, lim) && drained;
-            if (vfill & (1u << st)) drained = mbar_wait_bounded(&sm.v_full[st], (vpar >> st) & 1u, lim) && drained;
-        }
+        bool drained = IS_K ? mbar_wait_bounded(&sm.q_full, 0, lim) : true;
+        for (int st = 0; st < Shape::NSTAGE; ++st)
+            if (fill & (1u << st)) drained = mbar_wait_bounded(&full[st], (par >> st) & 1u, lim) && drained;
         if (!drained) set_error(p.err, PA_DEVERR_TIMEOUT);
     }
     __syncwarp();
@@ -241,38 +238,43 @@ __device__ void prefill_mma(const PrefillParams& p, typename Shape::Smem& sm, ui
     constexpr int KS_S = Shape::SLABS * 4;  // 16-element steps over head_dim
     constexpr int KS_O = Shape::BN / 16;    // 16-position steps over the tile
     const uint64_t lim = p.wait_limit_ns;
-    const uint32_t q_base = smem_addr(sm.q[0]);
+    // Every operand sits at a fixed shared-memory address: descriptor bases
+    // are computed once and each MMA adds a compile-time offset (the start
+    // address field is the low 14 bits, address / 16, below 2^14).
+    constexpr uint64_t STAGE16 = sizeof(sm.k[0]) >> 4;  // descriptor step between stages
+    const uint64_t dq = smem_desc_sw128(smem_addr(sm.q[0]), 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(smem_addr(sm.k[0][0]), 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(smem_addr(sm.v[0][0]), Shape::KV_SLAB, 1024);
 
     // S_js = Q K_js^T into buffer js % 2; the K slot is released when it completes.
     auto issue_s = [&](int js) {
         const int b = js & 1, st = js % Shape::NSTAGE;
-        const uint32_t k_base = smem_addr(sm.k[st][0]);
+        const uint64_t dk = dk0 + (uint64_t)st * STAGE16;
 #pragma unroll
         for (int ks = 0; ks < KS_S; ++ks)
-            mma_f16_ss(tmem + b * Shape::BN,
-                       smem_desc_sw128(q_base + (ks >> 2) * Shape::Q_SLAB + (ks & 3) * 32, 16, 1024),
-                       smem_desc_sw128(k_base + (ks >> 2) * Shape::KV_SLAB + (ks & 3) * 32, 16, 1024), IDESC_S,
+            mma_f16_ss(tmem + b * Shape::BN, dq + (uint64_t)((ks >> 2) * (Shape::Q_SLAB >> 4) + (ks & 3) * 2),
+                       dk + (uint64_t)((ks >> 2) * (Shape::KV_SLAB >> 4) + (ks & 3) * 2), IDESC_S,
                        ks > 0 ? 1u : 0u);
         mma_commit(&sm.s_full[b]);
         mma_commit(&sm.k_empty[st]);
     };
     // O += P_jp V_jp: A = P from TMEM (8 columns per 16 positions), B = V
-    // MN-major (head_dim along N, slabs Shape::KV_SLAB bytes apart).  With
-    // SPLIT_P the 16-bit P is P_hi + P_lo and both halves are multiplied.
+    // MN-major (head_dim along N, slabs Shape::KV_SLAB bytes apart; rows
+    // 16 ks .. 16 ks + 15 start 2048 bytes apart).  With SPLIT_P the 16-bit
+    // P is P_hi + P_lo and both halves are multiplied.
     auto issue_pv = [&](int jp) {
         const int b = jp & 1, st = jp % Shape::NSTAGE;
-        const uint32_t v_base = smem_addr(sm.v[st][0]);
+        const uint64_t dv = dv0 + (uint64_t)st * STAGE16;
         const uint32_t p_tmem = tmem + b * Shape::BN;
+        const uint32_t acc0 = jp > 0 ? 1u : 0u;
 #pragma unroll
         for (int ks = 0; ks < KS_O; ++ks)
-            mma_f16_ts(tmem + Shape::O_COL, p_tmem + ks * 8,
-                       smem_desc_sw128(v_base + ks * 16 * 128, Shape::KV_SLAB, 1024), IDESC_O,
-                       (jp > 0 || ks > 0) ? 1u : 0u);
+            mma_f16_ts(tmem + Shape::O_COL, p_tmem + ks * 8, dv + (uint64_t)ks * 128, IDESC_O, ks > 0 ? 1u : acc0);
         if constexpr (SPLIT_P) {
 #pragma unroll
             for (int ks = 0; ks < KS_O; ++ks)
-                mma_f16_ts(tmem + Shape::O_COL, p_tmem + Shape::BN / 2 + ks * 8,
-                           smem_desc_sw128(v_base + ks * 16 * 128, Shape::KV_SLAB, 1024), IDESC_O, 1u);
+                mma_f16_ts(tmem + Shape::O_COL, p_tmem + Shape::BN / 2 + ks * 8, dv + (uint64_t)ks * 128, IDESC_O,
+                           1u);
         }
         mma_commit(&sm.pv_done[b]);
         mma_commit(&sm.v_empty[st]);
@@ -552,8 +554,10 @@ __global__ void __launch_bounds__(PrefillShape<D>::THREADS, PrefillShape<D>::CTA
     tc_fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == Shape::PRODUCER_WARP) {
-        prefill_producer<Shape>(p, sm, lane, w, &tmap_q, &tmap_k, &tmap_v);
+    if (warp == Shape::K_WARP) {
+        prefill_producer<Shape, true>(p, sm, lane, w, &tmap_q, &tmap_k);
+    } else if (warp == Shape::V_WARP) {
+        prefill_producer<Shape, false>(p, sm, lane, w, &tmap_q, &tmap_v);
     } else if (warp == Shape::MMA_WARP) {
         if (lane == 0) prefill_mma<Shape, IDESC_S, IDESC_O, BF16>(p, sm, tmem, w.nt);
         __syncwarp();
