@@ -22,6 +22,13 @@ steps.
 
 --impl reference runs the fp64 CPU oracle on the same workload (a bounded
 sample of sequences per step) as the comparison arm.
+
+--workload prefill_llama8b / prefill_opt13b times the prompt phase over a
+cached shared prefix instead: one step is the copy-on-write of the shared
+partial block, the cache write of every new token and pa_prefill; the metric
+is useful attention TFLOP/s (causal pairs only) against the measured bf16
+tensor peak.  The default run also reports both prefill workloads under
+"rows".
 """
 from __future__ import annotations
 
@@ -45,6 +52,7 @@ from paged_kv_cache_132_gb300 import api, metrics, native, workloads  # noqa: E4
 WORKLOAD = "llama8b"
 METRIC = "paged decode-attention KV GB/s (% of GB300 HBM peak); seq-decode-steps/s"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_llama8b_ncu.md")
+PREFILL_METRIC = "paged prefill attention TFLOP/s (useful, causal pairs; % of GB300 bf16 tensor peak); new tokens/s"
 KERNEL_SOURCES = ["decode_mma.cuh", "decode_common.cuh", "decode.cu", "common.cuh"]
 
 
@@ -56,8 +64,10 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle leg")
-    ap.add_argument("--workload", choices=list(workloads.WORKLOADS) + ["beam_search"], default=WORKLOAD,
-                    help="which synthetic workload one step runs over (default: the Llama-8B-shaped batch)")
+    ap.add_argument("--workload", choices=list(workloads.WORKLOADS) + ["beam_search"] + list(workloads.PREFILL_WORKLOADS),
+                    default=WORKLOAD,
+                    help="which synthetic workload one step runs over (default: the Llama-8B-shaped batch); "
+                         "prefill_*: prompt-phase attention over a cached shared prefix")
     ap.add_argument("--block-size", type=int, default=16, help="long_context sweep point (8, 16 or 32)")
     ap.add_argument("--partition-size", type=int, default=None,
                     help="split-KV partition (default: the workload's, else 512)")
@@ -224,8 +234,41 @@ def cpu_baseline(w, target_seconds):
                       f"OpenMP over (sequence, KV head), {total_t:.1f} s"}
 
 
+def run_reference_prefill(args):
+    """The oracle's prefill on the same step: each timed step is a bounded
+    sample (whole sequences, shortest first) sized so that warm-up + timed
+    steps take about two minutes."""
+    st = workloads.make_prefill(args.workload, device="cpu", num_seqs=args.num_seqs)
+    per_step = max(0.05, 120.0 / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        prefill_cpu_baseline(st, per_step)
+    tot_t = tot_f = 0.0
+    last = None
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        last = prefill_cpu_baseline(st, per_step)
+        dt = time.perf_counter() - t0
+        tot_t += dt
+        tot_f += last["value"] * 1e12 * dt
+    value = tot_f / tot_t / 1e12
+    dt_name = {torch.float16: "f16", torch.bfloat16: "bf16"}[st.dtype]
+    print(json.dumps({"impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s",
+                      "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": 1e3 * tot_t / max(args.steps, 1), "higher_is_better": True, "scaling": "weak",
+                      "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                      "config": {"workload": f"{st.name}: {st.num_seqs} requests, {st.num_heads} query / "
+                                             f"{st.num_kv_heads} KV heads, d {st.head_dim}, {dt_name} inputs"},
+                      "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
+                                       "sample": last["sample"]},
+                      "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                              "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
+        return
+    if args.workload.startswith("prefill_"):
+        run_reference_prefill(args)
         return
     import numpy as np
 
@@ -536,6 +579,7 @@ def run_ours(args, rank, world, local_rank):
         rows["a7_copy_blocks_graph_pairs"] = int(ps.copy_pairs.shape[0])
         del ps, ck, cv
         rows.update(swap_rows(w, stream))
+        rows.update(prefill_rows(stream))
 
     # ---- CPU oracle baseline (rank 0, one GPU only) ------------------------
     cpu = None
@@ -578,6 +622,209 @@ def run_ours(args, rank, world, local_rank):
             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "host_us_per_step": host_us},
         "gpu_launches": launches,
         "gpu_launches_e2e": launches_e2e,
+        "clocks": clocks,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# prefill over a cached shared prefix
+# ---------------------------------------------------------------------------
+def prefill_step_fn(st, k, v, out):
+    """The step: copy-on-write, cache write of the new tokens, prefill."""
+    def step():
+        if st.copy_pairs.numel():
+            api.copy_blocks([k], [v], st.copy_pairs)
+        api.reshape_and_cache(st.new_key, st.new_value, k, v, st.slot_mapping)
+        api.prefill(st.query, st.query_start_loc, k, v, st.block_tables, st.context_lens, st.scale,
+                    st.max_query_len, out=out)
+    return step
+
+
+def prefill_rows(stream, names=("prefill_llama8b", "prefill_opt13b")):
+    """Each prefill workload's pa_prefill call and whole step, timed from CUDA
+    graphs; useful TFLOP/s and its fraction of the measured bf16 peak."""
+    peaks, kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    rows = {}
+    for name in names:
+        st = workloads.make_prefill(name, device="cuda")
+        k, v = st.k_cache.clone(), st.v_cache.clone()
+        out = torch.empty(st.num_tokens, st.num_heads, st.head_dim, dtype=st.dtype, device="cuda")
+        prefill_step_fn(st, k, v, out)()
+        call_us = graph_time_us(lambda: api.prefill(st.query, st.query_start_loc, k, v, st.block_tables,
+                                                    st.context_lens, st.scale, st.max_query_len, out=out),
+                                10, stream)
+        step_us = graph_time_us(prefill_step_fn(st, k, v, out), 10, stream)
+        status, code = api.get_device_error()
+        if status != 0:
+            raise RuntimeError(f"device error {status} ({code:#x}) in the {name} row")
+        tflops = metrics.prefill_flops(st.attended_pairs(), st.num_heads, st.head_dim) / (call_us * 1e-6) / 1e12
+        rows[f"{name}_call_us"] = call_us
+        rows[f"{name}_tflops"] = tflops
+        rows[f"{name}_frac_of_{kind}_bf16_peak"] = tflops / peak
+        rows[f"{name}_step_us"] = step_us
+        rows[f"{name}_new_tokens_per_s"] = st.num_tokens / (step_us * 1e-6)
+        del st, k, v, out
+    return rows
+
+
+def prefill_cpu_baseline(st, target_seconds):
+    """The fp64 oracle on whole sequences of the step, as many as fit in
+    about target_seconds (at least one)."""
+    import numpy as np
+
+    import oracle as O
+
+    def bits(t):
+        t = t.detach().contiguous().cpu()
+        return t.view(torch.int16).numpy()
+
+    orc = O.get()
+    threads = orc.max_threads()
+    code = {torch.float16: O.F16, torch.bfloat16: O.BF16}[st.dtype]
+    k, v = bits(st.k_cache).copy(), bits(st.v_cache).copy()
+    if st.copy_pairs.numel():
+        orc.copy_blocks([k], [v], st.copy_pairs.cpu().numpy())
+    orc.reshape_and_cache(bits(st.new_key), bits(st.new_value), k, v, st.slot_mapping.cpu().numpy())
+    q = bits(st.query)
+    qsl = st.query_start_loc.cpu().numpy()
+    tables, ctx = st.block_tables.cpu().numpy(), st.context_lens.cpu().numpy()
+    total_t, flops, done = 0.0, 0, 0
+    order = np.argsort(np.asarray(st.chunk_lens))  # shortest first: several sequences in the budget
+    for s in order:
+        a, b = int(qsl[s]), int(qsl[s + 1])
+        if b == a:
+            continue
+        t0 = time.perf_counter()
+        orc.prefill(q[a:b], np.array([0, b - a], dtype=np.int32), k, v, code, tables[s:s + 1], ctx[s:s + 1],
+                    st.num_kv_heads, st.scale, num_threads=threads)
+        total_t += time.perf_counter() - t0
+        n, pre = st.chunk_lens[s], st.prefix_lens[s]
+        flops += metrics.prefill_flops(n * pre + n * (n + 1) // 2, st.num_heads, st.head_dim)
+        done += 1
+        if total_t >= target_seconds:
+            break
+    return {"value": flops / total_t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{done} whole sequence(s) of the step (shortest first), fp64, OpenMP over KV heads, "
+                      f"{total_t:.1f} s"}
+
+
+def run_prefill(args, rank, world, local_rank):
+    """One step: copy-on-write of the shared partial prefix block, cache write
+    of the new tokens, pa_prefill.  value = useful attention TFLOP/s of the
+    step (whole job); roofline = the pa_prefill call against the measured
+    bf16 tensor peak."""
+    torch.cuda.set_device(local_rank)
+    native.load()
+    st = workloads.make_prefill(args.workload, device="cuda", num_seqs=args.num_seqs,
+                                seed=None if rank == 0 else workloads.SEED_BASE + 500 + rank)
+    stream = torch.cuda.current_stream()
+    k, v = st.k_cache.clone(), st.v_cache.clone()
+    out = torch.empty(st.num_tokens, st.num_heads, st.head_dim, dtype=st.dtype, device="cuda")
+    step = prefill_step_fn(st, k, v, out)
+    flops = metrics.prefill_flops(st.attended_pairs(), st.num_heads, st.head_dim)
+    n_pairs = int(st.copy_pairs.shape[0])
+    per_step = (1 if n_pairs else 0) + 2
+    for _ in range(max(args.warmup, 3)):
+        step()
+    status, code = api.get_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error {status} ({code:#x}) during warm-up")
+    k_steps = max(1, args.steps)
+    sampler = ClockSampler(local_rank)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)
+    s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(k_steps):
+        step()
+    e0.record(stream)
+    torch.cuda.synchronize()
+    # breakdown: the pa_prefill call alone, events around each call
+    calls = []
+    for _ in range(min(k_steps, 50)):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if n_pairs:
+            api.copy_blocks([k], [v], st.copy_pairs)
+        api.reshape_and_cache(st.new_key, st.new_value, k, v, st.slot_mapping)
+        a.record(stream)
+        api.prefill(st.query, st.query_start_loc, k, v, st.block_tables, st.context_lens, st.scale,
+                    st.max_query_len, out=out)
+        b.record(stream)
+        calls.append((a, b))
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    status, code = api.get_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error {status} ({code:#x}) in the timed region")
+    step_ms = all_reduce_max(s0.elapsed_time(e0) / k_steps, world)
+    call_ms = statistics.median(a.elapsed_time(b) for a, b in calls)
+
+    # end to end: the step's inputs from page-locked host memory, the output back
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.cpu().pin_memory() for t in (st.query, st.new_key, st.new_value, st.slot_mapping,
+                                                   st.query_start_loc, st.context_lens, st.block_tables)]
+        dev_in = [st.query, st.new_key, st.new_value, st.slot_mapping, st.query_start_loc, st.context_lens,
+                  st.block_tables]
+        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = host_out.numel() * host_out.element_size()
+
+        def e2e_step():
+            for h, d in zip(host_in, dev_in):
+                d.copy_(h, non_blocking=True)
+            step()
+            host_out.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(1, min(k_steps, 200))
+        s1, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s1.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = all_reduce_max(s1.elapsed_time(e1) / n_e2e, world)
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = prefill_cpu_baseline(st, args.cpu_seconds)
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    achieved = flops / (call_ms * 1e-3) / 1e12
+    dt = {torch.float16: "f16", torch.bfloat16: "bf16"}[st.dtype]
+    line = {
+        "metric": PREFILL_METRIC,
+        "value": world * flops / (step_ms * 1e-3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world, "steps": k_steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "config": {"workload": f"{st.name}: {st.num_seqs} requests, prefixes {sorted(set(st.prefix_lens))}, "
+                               f"{st.num_tokens} new tokens (max chunk {st.max_query_len}), {st.num_heads} query / "
+                               f"{st.num_kv_heads} KV heads, d {st.head_dim}, {dt}, block {st.block_size}, "
+                               f"{n_pairs} copy-on-write pairs",
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (queries + outputs + pool above 129 MB); no flush",
+                   "useful_flops_per_step": flops, "attended_pairs_per_head": st.attended_pairs()},
+        "new_tokens_per_s": world * st.num_tokens / (step_ms * 1e-3),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": None, "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                     "kernel": "pa_prefill (tcgen05 kernel), CUDA events per call; bf16 P is split in two halves, "
+                               "so the tensor pipe does 1.5x the useful flops"},
+        "rows": {"prefill_call_us": 1e3 * call_ms, "step_us": 1e3 * step_ms},
+        "e2e": e2e,
+        "gpu_launches": k_steps * per_step,
         "clocks": clocks,
     }
     if cpu is not None:
@@ -686,6 +933,8 @@ def main():
     try:
         if args.workload == "beam_search":
             run_beam(args, rank, world, local_rank)
+        elif args.workload.startswith("prefill_"):
+            run_prefill(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

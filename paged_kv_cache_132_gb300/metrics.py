@@ -53,3 +53,18 @@ def copy_bytes(num_pairs: int, num_layers: int, num_kv_heads: int, block_size: i
                elem_bytes: int) -> int:
     """Read + write of the K and V block of every pair and layer."""
     return 2 * 2 * num_pairs * num_layers * num_kv_heads * block_size * head_dim * elem_bytes
+
+
+def prefill_flops(attended_pairs: int, num_heads: int, head_dim: int) -> int:
+    """Useful flops of prefill attention: for every (query head, new token,
+    attended position) pair, 2 d for q.k and 2 d for the weighted sum of v
+    (positions the causal mask excludes are not counted)."""
+    return 4 * head_dim * num_heads * int(attended_pairs)
+
+
+def prefill_bytes(num_tokens: int, num_heads: int, kv_positions: int, num_kv_heads: int, head_dim: int,
+                  elem_bytes: int, out_bytes: int) -> int:
+    """Compulsory bytes of one prefill call: the queries, the outputs and each
+    distinct K/V row read once (kv_positions = distinct cached positions)."""
+    return num_tokens * num_heads * head_dim * (elem_bytes + out_bytes) + \
+        2 * kv_positions * num_kv_heads * head_dim * elem_bytes
