@@ -229,9 +229,18 @@ def cpu_baseline(w, target_seconds):
         total_t += dt
         total_b += nb
         passes += 1
+    # the same oracle on one thread, on the first sequences of the batch (~2 s)
+    one_t = one_b = 0.0
+    for s_ in range(w.num_seqs):
+        dt, nb = oracle_run(setup, w, np.array([s_]), 1)
+        one_t += dt
+        one_b += nb
+        if one_t >= 2.0:
+            break
     return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{passes} full pass(es) of the {w.num_seqs}-sequence batch, fp64, "
-                      f"OpenMP over (sequence, KV head), {total_t:.1f} s"}
+                      f"OpenMP over (sequence, KV head), {total_t:.1f} s",
+            "single_thread_gbs": one_b / one_t / 1e9, "nproc": os.cpu_count()}
 
 
 def run_reference_prefill(args):
@@ -563,7 +572,25 @@ def run_ours(args, rank, world, local_rank):
         launches_e2e = k_e2e * per_step
 
     rows = {"a1_cache_write_us": 1e3 * write_ms, "a2_a6_decode_us": 1e3 * decode_ms,
+            "a1_cache_write_median_us": 1e3 * statistics.median(e[1].elapsed_time(e[2]) for e in ev),
+            "a2_a6_decode_median_us": 1e3 * statistics.median(e[2].elapsed_time(e[3]) for e in ev),
             "step_graph_us": graph_time_us(step, 20, stream)}
+    if not args.no_rows:
+        # ---- cold decode calls: L2 flushed (a 2 x L2 buffer written) before each
+        flush = torch.empty(2 * 129 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+        cold = []
+        for _ in range(20):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            api.decode(w.query, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, out=out,
+                       max_context_len=max_ctx, partition_size=part, workspace=ws)
+            b.record(stream)
+            cold.append((a, b))
+        torch.cuda.synchronize()
+        rows["a2_a6_decode_cold_median_us"] = 1e3 * statistics.median(a.elapsed_time(b) for a, b in cold)
+        rows["a2_a6_decode_cold_gbs"] = decode_b / (rows["a2_a6_decode_cold_median_us"] * 1e-6) / 1e9
+        del flush
     if n_pairs:
         rows["a7_copy_blocks_us"] = 1e3 * copy_ms
         rows["a7_copy_blocks_pairs"] = n_pairs
@@ -610,7 +637,8 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic",
         "config": {"workload": desc, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (KV bytes per step far above the 129 MB L2); no flush",
-                   "algorithmic_bytes_per_step": bytes_step, "sum_context_tokens": int(sum(ctx_list))},
+                   "algorithmic_bytes_per_step": bytes_step, "sum_context_tokens": int(sum(ctx_list)),
+                   "table_and_length_bytes_per_step": metrics.table_bytes(ctx_list, w.block_size)},
         "seq_decode_steps_per_s": world * w.num_seqs / (step_ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
