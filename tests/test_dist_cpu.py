@@ -41,7 +41,10 @@ def _worker(rank, world, port, results):
 
 def test_two_rank_replicas_take_the_slowest_time():
     world = 2
-    results = mp.Manager().dict()
+    # the manager process is spawned too: forking a process that already
+    # runs threads can deadlock the child
+    manager = mp.get_context("spawn").Manager()
+    results = manager.dict()
     mp.spawn(_worker, args=(world, _free_port(), results), nprocs=world, join=True)
     (slow0, ctx0, n0), (slow1, ctx1, n1) = results[0], results[1]
     assert slow0 == slow1 == 2.0
