@@ -4,6 +4,8 @@ Cache writes and block copies must match bit for bit over the whole pool;
 attention outputs must be within 2e-3 absolute (fp32 output), or 2e-3 plus
 half an ulp of the output type.  Workloads fill every stale slot with NaN.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -81,6 +83,18 @@ def test_output_in_query_dtype(kernel):
 def test_forced_partitions(partition, kernel):
     w = workloads.make("llama8b", device="cuda", num_seqs=48)
     _check_step(w, partition_size=partition)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=str)
+def test_large_scores(dtype, kernel):
+    """A softmax scale 40 times 1/sqrt(d): scores spread over hundreds of
+    units, so a row's running max grows many times along the context (every
+    rescaling path runs) and the weights are nearly one-hot."""
+    w = workloads.custom([1, 40, 300, 777, 2048, 3000], num_heads=32, num_kv_heads=8, head_dim=128,
+                         block_size=16, dtype=dtype, num_blocks=None, device="cuda", seed=7400)
+    w = dataclasses.replace(w, scale=w.scale * 40.0)
+    for partition in (0, 512):
+        _check_step(w, partition_size=partition)
 
 
 LENGTHS = [0, 1, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 129, 200, 513]

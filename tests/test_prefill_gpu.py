@@ -6,6 +6,8 @@ of the new tokens, then pa_prefill.  Pools must match the oracle bit for bit;
 attention outputs within 2e-3 absolute (plus half an ulp of a 16-bit output
 type).  Every slot that holds no cached token is NaN.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -109,6 +111,17 @@ def test_prefill_shapes(dtype, d, h, hkv, bs):
                                   num_heads=h, num_kv_heads=hkv, head_dim=d, block_size=bs, dtype=dtype,
                                   seed=7100 + d + h + bs, device="cuda")
     check(st)
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float16, 128), (torch.bfloat16, 64)])
+def test_prefill_large_scores(dtype, d):
+    """A softmax scale 40 times 1/sqrt(d): a row's running max grows many
+    times along the keys (the rescaling of O, and of P inside a tile, runs)
+    and the weights are nearly one-hot."""
+    st = workloads.prefill_custom([1, 77, 300, 129], [0, 45, 1000], prefix_groups=[1, 0, 2, 2],
+                                  num_heads=16, num_kv_heads=4, head_dim=d, block_size=16, dtype=dtype,
+                                  seed=7500 + d, device="cuda")
+    check(dataclasses.replace(st, scale=st.scale * 40.0))
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float16, torch.bfloat16])
