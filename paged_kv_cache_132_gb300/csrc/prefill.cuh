@@ -406,24 +406,25 @@ __device__ void prefill_softmax(const PrefillParams& p, typename Shape::Smem& sm
         l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
 
         // P over S in TMEM.  bf16: P = P_hi + P_lo, both truncated to 16 bits
-        // (relative error below 2^-14); f16: P rounded once (2^-11).
+        // (relative error below 2^-14); f16: P rounded once (2^-11).  The
+        // stores complete before P's arrival is signalled (one wait below).
         {
             uint32_t u[BN / 2];
             if constexpr (SPLIT_P) {
 #pragma unroll
                 for (int k = 0; k < BN / 2; ++k) u[k] = pack_hi_halves(x[2 * k], x[2 * k + 1]);
-                tmem_st_x32(row_addr + b * BN, u);
+                tmem_st_x32_async(row_addr + b * BN, u);
 #pragma unroll
                 for (int k = 0; k < BN / 2; ++k) {
                     const float a = x[2 * k] - __uint_as_float(__float_as_uint(x[2 * k]) & 0xffff0000u);
                     const float e = x[2 * k + 1] - __uint_as_float(__float_as_uint(x[2 * k + 1]) & 0xffff0000u);
                     u[k] = pack_hi_halves(a, e);
                 }
-                tmem_st_x32(row_addr + b * BN + BN / 2, u);
+                tmem_st_x32_async(row_addr + b * BN + BN / 2, u);
             } else {
 #pragma unroll
                 for (int k = 0; k < BN / 2; ++k) u[k] = pack_rn<T>(x[2 * k], x[2 * k + 1]);
-                tmem_st_x32(row_addr + b * BN, u);
+                tmem_st_x32_async(row_addr + b * BN, u);
             }
         }
 
@@ -463,6 +464,7 @@ __device__ void prefill_softmax(const PrefillParams& p, typename Shape::Smem& sm
                 tmem_st_x32(row_addr + Shape::O_COL + c0, u);
             }
         }
+        tmem_wait_st();
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.p_full[b]);
