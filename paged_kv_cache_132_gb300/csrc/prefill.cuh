@@ -318,6 +318,33 @@ __device__ void prefill_mma(const PrefillParams& p, typename Shape::Smem& sm, ui
 // ---------------------------------------------------------------------------
 // softmax warps (thread r = row r = TMEM lane r)
 // ---------------------------------------------------------------------------
+// Packed pairs of binary32 (Blackwell f32x2 arithmetic): each half is
+// rounded to nearest like the scalar instruction, two results per issue.
+// (x0, x1) = (x0 * a0 + b0, x1 * a1 + b1)
+__device__ __forceinline__ void fma2_rn(float& x0, float& x1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 x, a, b;\n\t"
+        "mov.b64 x, {%0, %1};\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "fma.rn.f32x2 x, x, a, b;\n\tmov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(x0), "+f"(x1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// (x0, x1) += (y0, y1)
+__device__ __forceinline__ void add2_rn(float& x0, float& x1, float y0, float y1) {
+    asm("{\n\t.reg .b64 x, y;\n\t"
+        "mov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+        "add.rn.f32x2 x, x, y;\n\tmov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(x0), "+f"(x1)
+        : "f"(y0), "f"(y1));
+}
+// (x0, x1) -= (y0, y1)
+__device__ __forceinline__ void sub2_rn(float& x0, float& x1, float y0, float y1) {
+    asm("{\n\t.reg .b64 x, y;\n\t"
+        "mov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+        "sub.rn.f32x2 x, x, y;\n\tmov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(x0), "+f"(x1)
+        : "f"(y0), "f"(y1));
+}
+
 // Two 16-bit values in one 32-bit word, the first in the low half.
 __device__ inline uint32_t pack_hi_halves(float a, float b) {
     // the high 16 bits of each binary32: bfloat16 truncation
@@ -394,15 +421,18 @@ __device__ void prefill_softmax(const PrefillParams& p, typename Shape::Smem& sm
             m = m_new;
             l *= alpha;
         }
+        // Exponent arguments and row sum two positions per instruction
+        // (packed f32x2 FMA / add, each half rounded as its scalar form).
         const float nm = -m;
+#pragma unroll
+        for (int k = 0; k < BN; k += 2) fma2_rn(x[k], x[k + 1], c, c, nm, nm);
+#pragma unroll
+        for (int k = 0; k < BN; ++k) x[k] = exp2_approx(x[k]);
         float ps[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) ps[q] = 0.f;
+        for (int q = 0; q < 8; ++q) ps[q] = x[q];
 #pragma unroll
-        for (int k = 0; k < BN; ++k) {
-            x[k] = exp2_approx(fmaf(x[k], c, nm));
-            ps[k & 7] += x[k];
-        }
+        for (int k = 8; k < BN; k += 2) add2_rn(ps[k & 7], ps[(k & 7) + 1], x[k], x[k + 1]);
         l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
 
         // P over S in TMEM.  bf16: P = P_hi + P_lo, both truncated to 16 bits
@@ -416,8 +446,10 @@ __device__ void prefill_softmax(const PrefillParams& p, typename Shape::Smem& sm
                 tmem_st_x32_async(row_addr + b * BN, u);
 #pragma unroll
                 for (int k = 0; k < BN / 2; ++k) {
-                    const float a = x[2 * k] - __uint_as_float(__float_as_uint(x[2 * k]) & 0xffff0000u);
-                    const float e = x[2 * k + 1] - __uint_as_float(__float_as_uint(x[2 * k + 1]) & 0xffff0000u);
+                    // P_lo = P - P_hi, exact: P_hi is P with its low 16 bits cleared
+                    float a = x[2 * k], e = x[2 * k + 1];
+                    sub2_rn(a, e, __uint_as_float(__float_as_uint(a) & 0xffff0000u),
+                            __uint_as_float(__float_as_uint(e) & 0xffff0000u));
                     u[k] = pack_hi_halves(a, e);
                 }
                 tmem_st_x32_async(row_addr + b * BN + BN / 2, u);
