@@ -54,6 +54,9 @@ METRIC = "paged decode-attention KV GB/s (% of GB300 HBM peak); seq-decode-steps
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_llama8b_ncu.md")
 PREFILL_METRIC = "paged prefill attention TFLOP/s (useful, causal pairs; % of GB300 bf16 tensor peak); new tokens/s"
 KERNEL_SOURCES = ["decode_mma.cuh", "decode_common.cuh", "decode.cu", "common.cuh"]
+PREFILL_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "prefill_llama8b_ncu.md")
+PREFILL_KERNEL_SOURCES = ["prefill.cuh", "prefill_launch.cuh", "prefill_bf16.cu", "tcgen05.cuh", "decode_common.cuh",
+                          "common.cuh"]
 
 
 def parse_args():
@@ -85,19 +88,21 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
-def kernel_digest() -> str:
+def kernel_digest(sources=None) -> str:
+    """Digest of a kernel's sources (default: the decode kernel's)."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, "paged_kv_cache_132_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current kernel source (digest line must match)."""
+def profiled_traffic(summary=PROFILE_SUMMARY, sources=None):
+    """DRAM bytes per launch of a kernel from its committed ncu summary (by
+    default the decode kernel's), if it was taken on the current kernel
+    source (digest line must match)."""
     try:
-        with open(PROFILE_SUMMARY, encoding="utf-8") as f:
+        with open(summary, encoding="utf-8") as f:
             text = f.read()
     except OSError:
         return None
@@ -107,7 +112,7 @@ def profiled_traffic():
             digest = line.split(":", 1)[1].strip()
         if line.startswith("dram_bytes_per_launch:"):
             traffic = float(line.split(":", 1)[1].strip())
-    return traffic if digest == kernel_digest() else None
+    return traffic if digest == kernel_digest(sources) else None
 
 
 def measured_peaks():
@@ -831,6 +836,10 @@ def run_prefill(args, rank, world, local_rank):
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", 1900.0))
     achieved = flops / (call_ms * 1e-3) / 1e12
+    # DRAM bytes per pa_prefill launch from the committed ncu summary (the
+    # llama8b-shaped workload at full size, current kernel source only)
+    traffic = (profiled_traffic(PREFILL_PROFILE_SUMMARY, PREFILL_KERNEL_SOURCES)
+               if args.workload == "prefill_llama8b" and args.num_seqs is None else None)
     dt = {torch.float16: "f16", torch.bfloat16: "bf16"}[st.dtype]
     line = {
         "metric": PREFILL_METRIC,
@@ -847,7 +856,7 @@ def run_prefill(args, rank, world, local_rank):
                    "useful_flops_per_step": flops, "attended_pairs_per_head": st.attended_pairs()},
         "new_tokens_per_s": world * st.num_tokens / (step_ms * 1e-3),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "traffic": None, "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                     "traffic": traffic, "peak_source": f"{peak_kind} bf16_tflops (burst)",
                      "kernel": "pa_prefill (tcgen05 kernel), CUDA events per call; bf16 P is split in two halves, "
                                "so the tensor pipe does 1.5x the useful flops"},
         "rows": {"prefill_call_us": 1e3 * call_ms, "step_us": 1e3 * step_ms},
