@@ -40,6 +40,10 @@ MUTANTS = {
     "prefill_position_off_by_one": ("int position = ctx - n + i;", "int position = ctx - n + i - 1;"),
     "prefill_query_row": ("int64_t row = (int64_t)(first + i) * num_heads + h;",
                           "int64_t row = (int64_t)(first + n - 1 - i) * num_heads + h;"),
+    "prefill_not_causal": ("Kc, Vc, position + 1, head_dim,", "Kc, Vc, ctx, head_dim,"),
+    "prefill_prefix_ignored": ("int position = ctx - n + i;", "int position = i;"),
+    "prefill_head_order": ("int h = kv_head * group + g;\n                    int64_t row = (int64_t)(first + i)",
+                           "int h = g * num_kv_heads + kv_head;\n                    int64_t row = (int64_t)(first + i)"),
     "max_not_subtracted_in_weights": ("z[j] = exp(z[j] - M); /* z now holds the unnormalised weights w_j */",
                                       "z[j] = exp(z[j] - M) * (j == 0 ? 2.0 : 1.0);"),
 }
