@@ -1,6 +1,6 @@
 // prefill_launch.cuh -- launch of one prefill kernel instance: one CTA per
-// (query tile, sequence, KV head), 192 threads, one CTA per SM, launched as a
-// programmatic dependent of the cache write before it.
+// (query tile, sequence, KV head), 224 threads, two CTAs per SM, launched as
+// a programmatic dependent of the cache write before it.
 #pragma once
 
 #include "prefill.cuh"
