@@ -417,8 +417,66 @@ def check_prefill_special_cases(orc):
         assert np.max(np.abs(got[qs[i]:qs[i + 1]] - ref[0].permute(1, 0, 2).numpy())) <= 1e-12
 
 
+def _numpy_step_pools(w):
+    """The pools after the step's copy-on-write copies and cache write, built
+    with numpy indexing alone (no oracle code): pairs in list order, then each
+    new token's rows at block slot // B, offset slot % B."""
+    b = w.block_size
+    k, v = bits(w.k_cache).copy(), bits(w.v_cache).copy()
+    for src, dst in w.copy_pairs.tolist():
+        k[dst] = k[src]
+        v[dst] = v[src]
+    nk, nv = bits(w.new_key), bits(w.new_value)
+    for t, slot in enumerate(w.slot_mapping.tolist()):
+        if slot >= 0:
+            k[slot // b, :, slot % b, :] = nk[t]
+            v[slot // b, :, slot % b, :] = nv[t]
+    return k, v
+
+
+def check_shared_prefix_equals_private_copies(orc):
+    """Invariant (3) of paging ("PagedAttention 论文精读笔记", §6.1 and §6.3:
+    sequences that share the physical blocks of a common prompt read exactly
+    what private copies would hold).  A parallel-sampling step (2 prompts x 8
+    samples sharing each 1000-token prompt, copy-on-write of the partial last
+    prompt block, per-sample tails) is decoded twice by the oracle: once on
+    its own step (its copy, its cache write, the shared tables), once with
+    every sequence given private copies of all the blocks it reads, built by
+    numpy indexing.  The outputs must be bit-identical."""
+    from paged_kv_cache_132_gb300 import workloads
+
+    w = workloads.make("parallel_sampling", device="cpu", num_seqs=16)
+    tables = w.block_tables.numpy()
+    ctx = w.context_lens.numpy()
+    b = w.block_size
+    used = [tables[s, : -(-int(ctx[s]) // b)] for s in range(w.num_seqs)]
+    counts = np.bincount(np.concatenate(used))
+    assert counts.max() >= 8, "the case must share prompt blocks"
+    code = code_of(w.dtype)
+    # shared: the oracle's whole step
+    k, v = bits(w.k_cache).copy(), bits(w.v_cache).copy()
+    orc.copy_blocks([k], [v], w.copy_pairs.numpy())
+    orc.reshape_and_cache(bits(w.new_key), bits(w.new_value), k, v, w.slot_mapping.numpy())
+    shared = orc.decode(bits(w.query), k, v, code, tables, ctx, w.num_kv_heads, w.scale)
+    # private: one fresh block per (sequence, logical block)
+    kn, vn = _numpy_step_pools(w)
+    total = sum(len(u) for u in used)
+    kp = np.empty((total,) + kn.shape[1:], dtype=kn.dtype)
+    vp = np.empty_like(kp)
+    ptab = np.full(tables.shape, -1, dtype=np.int32)
+    nxt = 0
+    for s, row in enumerate(used):
+        for j, blk in enumerate(row):
+            kp[nxt], vp[nxt] = kn[blk], vn[blk]
+            ptab[s, j] = nxt
+            nxt += 1
+    private = orc.decode(bits(w.query), kp, vp, code, ptab, ctx, w.num_kv_heads, w.scale)
+    assert np.all(np.isfinite(shared)), "a stale (NaN) slot reached a shared-prefix output"
+    assert np.array_equal(shared, private), "shared-prefix output differs from private copies"
+
+
 ORACLE_CHECKS = [check_sdpa, check_weight_sums, check_block_permutation, check_stale_slots_ignored,
                  check_gqa_equals_repeated_mha, check_closed_forms, check_partition_merge,
                  check_f16_decoding, check_bf16_decoding, check_swap_roundtrip,
-                 check_prefill_vs_sdpa, check_prefill_special_cases]
+                 check_prefill_vs_sdpa, check_prefill_special_cases, check_shared_prefix_equals_private_copies]
 GOLDEN_CHECKS = [check_walkthrough_write, check_figure6, check_address_lookup, check_copy_on_write]

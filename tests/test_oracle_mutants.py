@@ -77,3 +77,22 @@ def test_mutant_is_caught(name, golden, tmp_path):
                                 include_dir=os.path.dirname(oracle.SOURCE))
     failures = _run_checks(oracle.Oracle(lib), golden)
     assert failures, f"mutant {name} passed every pin"
+
+
+@pytest.mark.parametrize("name", ["copy_value_direction", "slot_block_offset_swapped"])
+def test_shared_prefix_pin_catches(name, tmp_path):
+    """The shared-prefix = private-copies pin on its own catches a copy in the
+    wrong direction and a slot split the wrong way round: the oracle's step
+    then disagrees with the numpy-built private pools.  (A wrong table index
+    reads the same wrong logical block through shared and private tables
+    alike; the SDPA and relabelling pins catch that one.)"""
+    original, mutated = MUTANTS[name]
+    with open(oracle.SOURCE, encoding="utf-8") as f:
+        text = f.read()
+    src = os.path.join(tmp_path, "mutant.c")
+    with open(src, "w", encoding="utf-8") as f:
+        f.write(text.replace(original, mutated))
+    lib = oracle.compile_oracle(src, os.path.join(tmp_path, "libmutant.so"),
+                                include_dir=os.path.dirname(oracle.SOURCE))
+    with pytest.raises((AssertionError, ValueError)):
+        pins.check_shared_prefix_equals_private_copies(oracle.Oracle(lib))
