@@ -4,9 +4,14 @@
 //    Management for Large Language Model Serving with PagedAttention Review",
 //    §3-2).  Each new token's K and V rows go straight from the projection
 //    layout [T][Hkv][d] into their slot of the block layout
-//    [NB][Hkv][B][d] in one pass, 16 bytes per thread, so that consecutive
-//    threads read consecutive bytes of the source and write whole rows of
-//    the destination.
+//    [NB][Hkv][B][d] in one pass.  A row (token, K|V, head) of d elements is
+//    C = d * e / 16 chunks of 16 bytes, handled by C consecutive lanes, so a
+//    warp reads consecutive bytes of the source and writes whole rows of the
+//    destination.  The row's indices and its slot are computed once per row
+//    (32-bit arithmetic), and every thread keeps four rows' loads in flight
+//    before it stores, which a bandwidth-bound copy of tens of MB needs.
+//    Rows whose C is not a power of two up to 32 take a plain grid-stride
+//    loop with one chunk per iteration.
 //  * block copies: "fused block copy for copy-on-write" (same page, §3-2;
 //    "PagedAttention 论文精读笔记", §6.1), and swapping between a GPU pool and
 //    a page-locked host pool (same notes, §7.4) -- the GPU reads and writes
@@ -20,6 +25,61 @@ namespace pa {
 namespace {
 
 constexpr int kWriteThreads = 256;
+constexpr int kWriteRowsInFlight = 4;
+
+// Rows r = (t * 2 + kv) * Hkv + h of T tokens, kv = 0 for K and 1 for V.
+// Thread (row group, lane c) handles chunk c of rows r0, r0 + R, ..., with R
+// the rows one pass of the CTA covers; 32-bit row indices (the host checks
+// 2 * T * Hkv < 2^31).
+__global__ void __launch_bounds__(kWriteThreads)
+reshape_and_cache_rows_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                              uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                              const int64_t* __restrict__ slot_mapping, int num_rows, int num_kv_heads,
+                              int block_size, int chunks_log2, int64_t num_slots, int* err) {
+    pdl_launch_dependents();  // as in the general kernel below
+    const int chunks = 1 << chunks_log2;
+    const int c = threadIdx.x & (chunks - 1);
+    const int rows_per_pass = kWriteThreads >> chunks_log2;
+    const int first = blockIdx.x * rows_per_pass * kWriteRowsInFlight + (threadIdx.x >> chunks_log2);
+    uint4 data[kWriteRowsInFlight];
+    int64_t slot[kWriteRowsInFlight];
+    int th[kWriteRowsInFlight];  // t * 2 + kv
+    int head[kWriteRowsInFlight];
+    // Loads of the source chunks and of the slots first, all independent...
+#pragma unroll
+    for (int u = 0; u < kWriteRowsInFlight; ++u) {
+        const int r = first + u * rows_per_pass;
+        slot[u] = -1;
+        if (r < num_rows) {
+            th[u] = (int)((unsigned)r / (unsigned)num_kv_heads);
+            head[u] = r - th[u] * num_kv_heads;
+            const int t = th[u] >> 1;
+            const uint4* src = (th[u] & 1) ? value : key;
+            data[u] = __ldcs(src + (((int64_t)t * num_kv_heads + head[u]) << chunks_log2) + c);
+            slot[u] = __ldg(slot_mapping + t);
+        }
+    }
+    // ...then the stores.
+#pragma unroll
+    for (int u = 0; u < kWriteRowsInFlight; ++u) {
+        const int64_t sl = slot[u];
+        if (sl < 0) continue;  // padding token (or no row): nothing to store
+        if (sl >= num_slots) {
+            if (c == 0 && head[u] == 0 && !(th[u] & 1)) set_error(err, PA_DEVERR_SLOT);
+            continue;
+        }
+        int64_t block, offset;
+        if (num_slots <= 0x7fffffffLL) {
+            block = (int64_t)((unsigned)sl / (unsigned)block_size);
+            offset = sl - block * block_size;
+        } else {
+            block = sl / block_size;
+            offset = sl - block * block_size;
+        }
+        uint4* dst = (th[u] & 1) ? v_cache : k_cache;
+        dst[((((block * num_kv_heads + head[u]) * block_size + offset)) << chunks_log2) + c] = data[u];
+    }
+}
 
 __global__ void __launch_bounds__(kWriteThreads)
 reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
@@ -120,7 +180,20 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k
                                      const PoolShape& shape, int* err, cudaStream_t stream) {
     if (num_tokens == 0) return cudaSuccess;
     const int chunks = shape.head_dim * shape.elem_bytes / 16;
-    const int64_t total = num_tokens * 2 * shape.num_kv_heads * chunks;
+    const int64_t rows = num_tokens * 2 * shape.num_kv_heads;
+    const bool pow2 = (chunks & (chunks - 1)) == 0 && chunks <= 32;
+    if (pow2 && rows < 0x7fffffffLL - kWriteThreads * kWriteRowsInFlight) {
+        int log2c = 0;
+        while ((1 << log2c) < chunks) ++log2c;
+        const int64_t rows_per_cta = (int64_t)(kWriteThreads >> log2c) * kWriteRowsInFlight;
+        const int64_t ctas = (rows + rows_per_cta - 1) / rows_per_cta;
+        reshape_and_cache_rows_kernel<<<(unsigned)ctas, kWriteThreads, 0, stream>>>(
+            static_cast<const uint4*>(key), static_cast<const uint4*>(value), static_cast<uint4*>(k_cache),
+            static_cast<uint4*>(v_cache), slot_mapping, (int)rows, shape.num_kv_heads, shape.block_size, log2c,
+            shape.num_blocks * shape.block_size, err);
+        return cudaGetLastError();
+    }
+    const int64_t total = rows * chunks;
     int64_t blocks = (total + kWriteThreads - 1) / kWriteThreads;
     if (blocks > 65536) blocks = 65536;  // grid-stride beyond this
     reshape_and_cache_kernel<<<(unsigned)blocks, kWriteThreads, 0, stream>>>(
