@@ -20,7 +20,9 @@
  *
  * Conventions shared by every call
  *   - Pointers named "device" are CUDA device pointers of the current device;
- *     the caller owns every buffer.  The library allocates no memory per call.
+ *     the caller owns every buffer.  The library allocates no memory per call
+ *     (its only device memory: one error word per device, and the fixed
+ *     array of pa_decode_noalloc).
  *   - Device data arrays (K/V, pools, queries, outputs) must be 16-byte
  *     aligned, index arrays aligned to their element size, and the decode
  *     workspace 256-byte aligned; anything else is PA_ERR_INVALID_ARG
@@ -47,7 +49,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 1
+#define PA_ABI_VERSION 2
 
 typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
 
@@ -68,6 +70,53 @@ typedef enum {
                                        or > the max_context_len the call was sized for    */
 #define PA_DEVERR_COPY_PAIR    0x8  /* copy or swap pair id outside its pool                */
 #define PA_DEVERR_TIMEOUT      0x10 /* a bounded wait inside a kernel ran out              */
+/* Reported only in checked mode (PA_OPT_DEBUG_CHECKS, below): */
+#define PA_DEVERR_DUP_SLOT     0x20 /* two tokens of one cache write share a slot          */
+#define PA_DEVERR_PAIR_CONFLICT 0x40 /* copy/swap pairs: a destination repeated, or (same
+                                        pool) a destination equal to its own or another
+                                        pair's source                                      */
+
+/*
+ * Library options, process-wide (every device, every thread).  Each starts
+ * from its environment variable, read once at the library's first call, and
+ * can be changed between calls with pa_set_option.  Calls read the options
+ * with plain atomic loads: no lock, no environment lookup per call.
+ *
+ *   PA_OPT_DEBUG_CHECKS (env PA_DEBUG_CHECKS=1): checked mode.  Before its
+ *     main kernel, each call below also launches a pre-pass that verifies the
+ *     preconditions the caller normally guarantees and reports violations
+ *     through the device error word -- never by trapping:
+ *       pa_reshape_and_cache  slot_mapping entries >= 0 distinct
+ *                             (PA_DEVERR_DUP_SLOT)
+ *       pa_copy_blocks        destinations distinct, no destination equal to
+ *                             any pair's source, its own included
+ *                             (PA_DEVERR_PAIR_CONFLICT)
+ *       pa_swap_blocks        destinations distinct; when the source and
+ *                             destination pools are the same memory, also as
+ *                             pa_copy_blocks (PA_DEVERR_PAIR_CONFLICT)
+ *       pa_decode(_noalloc)   0 <= context_lens[s] <= max_context_len and
+ *                             <= max_blocks_per_seq * block_size
+ *                             (PA_DEVERR_CONTEXT_LEN), every block id the
+ *                             sequence reads in [0, num_blocks)
+ *                             (PA_DEVERR_BLOCK_ID)
+ *     The main kernel then runs as usual: its result is unspecified where a
+ *     precondition is broken, but no access leaves the caller's buffers.
+ *     The pair and slot checks compare all pairs of entries: O(n^2) work,
+ *     meant for debugging, not for production batches.
+ *   PA_OPT_DECODE_KERNEL (env PA_DECODE_KERNEL=simt -> 1): decode kernel for
+ *     16-bit pools: 0 = tensor-core consumer (default), 1 = CUDA-core one.
+ *   PA_OPT_DROP_FIRST_FILL (env PA_DEBUG_DROP_FIRST_FILL=1): test hook of the
+ *     bounded waits -- every decode CTA leaves its first pipeline stage
+ *     unfilled, its wait runs out and the call reports PA_DEVERR_TIMEOUT.
+ */
+typedef enum { PA_OPT_DEBUG_CHECKS = 0, PA_OPT_DECODE_KERNEL = 1, PA_OPT_DROP_FIRST_FILL = 2 } pa_option;
+
+/* Sets `option` to `value` (0 or 1); returns its previous value, or
+ * PA_ERR_INVALID_ARG for an unknown option or value. */
+int pa_set_option(int option, int value);
+
+/* Current value of `option`, or PA_ERR_INVALID_ARG for an unknown one. */
+int pa_get_option(int option);
 
 /* Shape of one layer's KV pool (K and V pools have the same shape). */
 typedef struct {
@@ -137,8 +186,11 @@ int pa_decode(void *out, int32_t out_dtype, const void *query,
               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * Size of the device array pa_decode_noalloc uses as its workspace: 32 MiB,
- * reserved on every GPU that loads the library, until the process exits.
+ * Size of the device array pa_decode_noalloc uses as its workspace: 32 MiB
+ * on every GPU where the library's code is loaded, held until the process
+ * exits.  When CUDA loads modules lazily (the default since CUDA 12.2, see
+ * CUDA_MODULE_LOADING), the array is committed on a device at the first
+ * pa_decode_noalloc call there, not when the library is loaded.
  */
 #define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
@@ -150,12 +202,19 @@ int pa_decode(void *out, int32_t out_dtype, const void *query,
  * device memory.  The paper has no counterpart of this call; it exists for
  * those callers only.  The arguments mean what they mean for pa_decode; the
  * workspace is a fixed array of PA_NOALLOC_SCRATCH_BYTES inside the library.
- *   - Nothing is allocated: no cudaMalloc, no cudaFree, no allocator call.
- *   - A batch whose workspace (pa_decode_workspace_size) exceeds the array
- *     returns PA_ERR_WORKSPACE before anything is launched.
- *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make it before any stream
- *     capture.
+ *   - Nothing is allocated per call: no cudaMalloc, no cudaFree, no
+ *     allocator call.
+ *   - Set-up: the first call on a device (with that device current) looks
+ *     up the array's device address; with lazy module loading this is also
+ *     when CUDA commits the array's 32 MiB on that device.  So a caller that
+ *     reserves the rest of the GPU's memory for itself makes this first call
+ *     at start-up, before that reservation, and before any stream capture.
+ *     A call with num_seqs = 0 (and an otherwise valid `cache`) does only
+ *     this set-up and launches nothing.
+ *   - A batch whose workspace exceeds the array returns PA_ERR_WORKSPACE
+ *     before anything is launched.  The check uses the partition size the
+ *     call will actually run (the automatic choice included), so a batch is
+ *     refused only if pa_decode itself would need more than the array.
  *   - All calls share the array, which keeps the last call's contents (each
  *     call resets what it needs).  Calls whose work overlaps on the GPU --
  *     other streams or host threads -- race on it; serialise them.

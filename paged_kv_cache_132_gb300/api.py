@@ -7,8 +7,9 @@ PyTorch or the CPU.  PyTorch provides device memory and streams.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
-from typing import Optional, Sequence, Tuple
+from typing import Iterator, Optional, Sequence, Tuple
 
 import torch
 
@@ -215,3 +216,37 @@ def decode_noalloc(query: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
                                  block_tables.shape[1], context_lens.data_ptr(), s, int(max_context_len), h, hkv,
                                  float(scale), int(partition_size), _stream_ptr(stream)), "pa_decode_noalloc")
     return out
+
+
+OPTIONS = {"debug_checks": native.OPT_DEBUG_CHECKS, "decode_kernel_simt": native.OPT_DECODE_KERNEL,
+           "drop_first_fill": native.OPT_DROP_FIRST_FILL}
+
+
+def set_option(name: str, value: bool) -> bool:
+    """Set a process-wide library option (pa_set_option); returns the previous
+    value.  ``debug_checks``: checked mode (precondition pre-passes that report
+    violations through the error word); ``decode_kernel_simt``: CUDA-core
+    decode for 16-bit pools; ``drop_first_fill``: test hook of the bounded
+    waits."""
+    prev = native.load().pa_set_option(OPTIONS[name], 1 if value else 0)
+    if prev < 0:
+        raise PaError(prev, "pa_set_option")
+    return bool(prev)
+
+
+def get_option(name: str) -> bool:
+    value = native.load().pa_get_option(OPTIONS[name])
+    if value < 0:
+        raise PaError(value, "pa_get_option")
+    return bool(value)
+
+
+@contextlib.contextmanager
+def option(name: str, value: bool = True) -> Iterator[None]:
+    """``with api.option("debug_checks"):`` -- the option set for the block,
+    restored afterwards."""
+    prev = set_option(name, value)
+    try:
+        yield
+    finally:
+        set_option(name, prev)

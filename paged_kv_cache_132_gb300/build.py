@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB_DIR = os.path.join(HERE, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libpa.so")
-SOURCES = ["pa_api.cu", "cache_ops.cu", "decode.cu", "decode_f32.cu", "decode_simt_f16.cu", "decode_simt_bf16.cu",
+SOURCES = ["pa_api.cu", "cache_ops.cu", "checks.cu", "decode.cu", "decode_f32.cu", "decode_simt_f16.cu", "decode_simt_bf16.cu",
            "decode_mma_f16.cu", "decode_mma_bf16.cu", "pa_noalloc.cu", "prefill.cu", "prefill_f16.cu",
            "prefill_bf16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -30,7 +30,26 @@ cudaError_t launch_swap_blocks(void* const* src_k, void* const* src_v, int64_t s
                                void* const* dst_v, int64_t dst_num_blocks, int num_layers, const int64_t* pairs,
                                int64_t num_pairs, const PoolShape& shape, int* err, cudaStream_t stream);
 
+// ---- checked mode (checks.cu): precondition pre-passes -----------------------
+// Each reports violations through the error word and never traps; see the
+// PA_OPT_DEBUG_CHECKS paragraph of include/pa.h.
+cudaError_t launch_check_unique_slots(const int64_t* slot_mapping, int64_t num_tokens, int* err,
+                                      cudaStream_t stream);
+cudaError_t launch_check_pairs(const int64_t* pairs, int64_t num_pairs, bool same_pool, int* err,
+                               cudaStream_t stream);
+cudaError_t launch_check_decode_inputs(const int32_t* context_lens, const int32_t* block_tables, int num_seqs,
+                                       int max_blocks, int block_size, int max_context_len, int64_t num_blocks,
+                                       int* err, cudaStream_t stream);
+
 // ---- decode (decode_*.cu) ----------------------------------------------------
+// Partition size a pa_decode call runs with: partition_size itself when it is
+// not 0, else the automatic choice for this batch on the current device;
+// -1 if the device cannot be queried.  (pa_api.cu)
+int decode_partition(int64_t num_seqs, int num_kv_heads, int max_context_len, int partition_size);
+
+// Workspace bytes of a pa_decode call that runs with `partition`.  (pa_api.cu)
+size_t decode_workspace_bytes(int num_seqs, int num_heads, int max_context_len, int partition, int head_dim);
+
 // Everything one decode launch needs; passed by value as the kernel argument.
 struct DecodeParams {
     void* out;

@@ -1,13 +1,22 @@
 // pa_api.cu -- the C ABI declared in include/pa.h: argument checks, the
-// per-device error word, the partition choice, and the launches.
+// per-device error word, the library options, the partition choice, and the
+// launches.
 //
 // Every argument error is caught here, before anything reaches the GPU; the
 // kernels only report what depends on device data (ids, slots, lengths) or on
 // time (a bounded wait that ran out), through the error word.
+//
+// Host cost per call is kept small because decode runs once per layer per
+// step: per-device facts (error word address, SM count) are looked up once
+// and then read with atomic loads, options are atomics initialised once from
+// the environment, and the TMA descriptors of the pools are encoded once per
+// (pool, shape) and cached per host thread.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <cstdint>
@@ -25,11 +34,8 @@ __device__ int g_device_error;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-int* g_error_ptr[kMaxDevices] = {};
-int g_sm_count[kMaxDevices] = {};
-
-constexpr int kAutoPartitionSmall = 256;
-constexpr int kAutoPartition = 512;
+std::atomic<int*> g_error_ptr[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
 
 int current_device() {
     int dev = -1;
@@ -38,24 +44,51 @@ int current_device() {
 }
 
 int* error_word(int dev) {
+    int* p = g_error_ptr[dev].load(std::memory_order_acquire);
+    if (p) return p;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_error_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-        g_error_ptr[dev] = static_cast<int*>(p);
+    p = g_error_ptr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_device_error) != cudaSuccess) return nullptr;
+        p = static_cast<int*>(a);
+        g_error_ptr[dev].store(p, std::memory_order_release);
     }
-    return g_error_ptr[dev];
+    return p;
 }
 
 int sm_count(int dev) {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_sm_count[dev]) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        g_sm_count[dev] = n;
-    }
-    return g_sm_count[dev];
+    int n = g_sm_count[dev].load(std::memory_order_acquire);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+    g_sm_count[dev].store(n, std::memory_order_release);
+    return n;
 }
+
+// ---- library options ---------------------------------------------------------
+constexpr int kNumOptions = 3;
+std::atomic<int> g_option[kNumOptions];
+std::once_flag g_option_env_once;
+
+bool env_is(const char* name, const char* value) {
+    const char* v = std::getenv(name);
+    return v && std::strcmp(v, value) == 0;
+}
+
+int option(int id) {
+    std::call_once(g_option_env_once, [] {
+        g_option[PA_OPT_DEBUG_CHECKS].store(env_is("PA_DEBUG_CHECKS", "1") ? 1 : 0);
+        g_option[PA_OPT_DECODE_KERNEL].store(env_is("PA_DECODE_KERNEL", "simt") ? 1 : 0);
+        g_option[PA_OPT_DROP_FIRST_FILL].store(env_is("PA_DEBUG_DROP_FIRST_FILL", "1") ? 1 : 0);
+    });
+    return g_option[id].load(std::memory_order_relaxed);
+}
+
+// An NVTX range around each entry point (free when no tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 // Wall-time limit of every wait inside a kernel (environment variable
 // PA_WAIT_TIMEOUT_MS, default 2000 ms).
@@ -171,11 +204,61 @@ bool encode_query_map(CUtensorMap* map, const void* base, int dtype, int num_tok
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Decode consumer: PA_DECODE_KERNEL=simt selects the CUDA-core kernels for
-// 16-bit pools too (the tensor-core ones are the default there).
-pa::DecodeVariant requested_variant() {
-    const char* v = std::getenv("PA_DECODE_KERNEL");
-    return (v && std::strcmp(v, "simt") == 0) ? pa::kDecodeSimt : pa::kDecodeMma;
+// Cache of encoded tensor maps, per host thread (no lock).  An encoding is a
+// pure function of its key (base address, shape, dtype, view), so a cached
+// map is valid for as long as the key matches, whatever the caller did with
+// the memory in between.  Kernel parameters are copied at launch, so the
+// returned pointer is only used before the next lookup on this thread.
+struct MapKey {
+    int kind;  // 0: pool, 2-D view; 1: pool, decode's view; 2: query
+    int dtype;
+    const void* base;
+    int64_t a, b, c, d;
+    bool operator==(const MapKey& o) const {
+        return kind == o.kind && dtype == o.dtype && base == o.base && a == o.a && b == o.b && c == o.c && d == o.d;
+    }
+};
+struct MapSlot {
+    CUtensorMap map;  // 64-byte aligned type
+    MapKey key;
+    bool valid;
+};
+constexpr int kMapSlots = 16;
+thread_local MapSlot t_maps[kMapSlots];
+thread_local unsigned t_map_next = 0;
+
+const CUtensorMap* find_map(const MapKey& key) {
+    for (int i = 0; i < kMapSlots; ++i)
+        if (t_maps[i].valid && t_maps[i].key == key) return &t_maps[i].map;
+    return nullptr;
+}
+
+MapSlot& next_map_slot() {
+    MapSlot& slot = t_maps[t_map_next % kMapSlots];
+    ++t_map_next;
+    slot.valid = false;
+    return slot;
+}
+
+const CUtensorMap* pool_map(const void* base, int dtype, const pa::PoolShape& shape, bool interleave) {
+    const MapKey key{interleave ? 1 : 0, dtype, base, shape.num_blocks, shape.num_kv_heads, shape.block_size,
+                     shape.head_dim};
+    if (const CUtensorMap* m = find_map(key)) return m;
+    MapSlot& slot = next_map_slot();
+    if (!encode_pool_map(&slot.map, base, dtype, shape, interleave)) return nullptr;
+    slot.key = key;
+    slot.valid = true;
+    return &slot.map;
+}
+
+const CUtensorMap* query_map(const void* base, int dtype, int num_tokens, int num_heads, int head_dim, int group) {
+    const MapKey key{2, dtype, base, num_tokens, num_heads, head_dim, group};
+    if (const CUtensorMap* m = find_map(key)) return m;
+    MapSlot& slot = next_map_slot();
+    if (!encode_query_map(&slot.map, base, dtype, num_tokens, num_heads, head_dim, group)) return nullptr;
+    slot.key = key;
+    slot.valid = true;
+    return &slot.map;
 }
 
 int status_of(cudaError_t e) {
@@ -184,11 +267,45 @@ int status_of(cudaError_t e) {
     return PA_ERR_CUDA;
 }
 
+constexpr int kAutoPartitionSmall = 256;
+constexpr int kAutoPartition = 512;
+
 }  // namespace
+
+namespace pa {
+
+int decode_partition(int64_t num_seqs, int num_kv_heads, int max_context_len, int partition_size) {
+    if (partition_size != 0) return partition_size;
+    const int dev = current_device();
+    const int sms = dev < 0 ? 0 : sm_count(dev);
+    if (sms <= 0) return -1;
+    // Enough independent (sequence, KV head, partition) items to keep every
+    // SM busy through the tail; shorter partitions when the batch is small.
+    const int64_t units = num_seqs * num_kv_heads;
+    return units * max_parts_for(max_context_len, kAutoPartition) < 4LL * sms ? kAutoPartitionSmall
+                                                                             : kAutoPartition;
+}
+
+size_t decode_workspace_bytes(int num_seqs, int num_heads, int max_context_len, int partition, int head_dim) {
+    return decode_workspace_layout(num_seqs, num_heads, max_parts_for(max_context_len, partition), head_dim).total;
+}
+
+}  // namespace pa
 
 extern "C" {
 
 int pa_abi_version(void) { return PA_ABI_VERSION; }
+
+int pa_set_option(int opt, int value) {
+    if (opt < 0 || opt >= kNumOptions || (value != 0 && value != 1)) return PA_ERR_INVALID_ARG;
+    option(opt);  // the environment's value first, so that it never overrides this one
+    return g_option[opt].exchange(value);
+}
+
+int pa_get_option(int opt) {
+    if (opt < 0 || opt >= kNumOptions) return PA_ERR_INVALID_ARG;
+    return option(opt);
+}
 
 const char* pa_status_string(int status) {
     switch (status) {
@@ -206,6 +323,7 @@ const char* pa_status_string(int status) {
 int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
                          const int64_t* slot_mapping, int64_t num_tokens, const pa_cache_desc* cache,
                          void* stream) {
+    NvtxRange range("pa_reshape_and_cache");
     pa::PoolShape shape;
     int rc = check_cache(cache, &shape);
     if (rc != PA_OK) return rc;
@@ -218,6 +336,10 @@ int pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void
     if (dev < 0) return PA_ERR_CUDA;
     int* err = error_word(dev);
     if (!err) return PA_ERR_CUDA;
+    if (option(PA_OPT_DEBUG_CHECKS)) {
+        rc = status_of(pa::launch_check_unique_slots(slot_mapping, num_tokens, err, static_cast<cudaStream_t>(stream)));
+        if (rc != PA_OK) return rc;
+    }
     return status_of(pa::launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens, shape,
                                                   err, static_cast<cudaStream_t>(stream)));
 }
@@ -235,6 +357,7 @@ int pa_decode(void* out, int32_t out_dtype, const void* query, const void* k_cac
               const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len, int32_t num_heads,
               int32_t num_kv_heads, float scale, int32_t partition_size, void* workspace,
               size_t workspace_bytes, void* stream) {
+    NvtxRange range("pa_decode");
     pa::PoolShape shape;
     int rc = check_cache(cache, &shape);
     if (rc != PA_OK) return rc;
@@ -254,18 +377,10 @@ int pa_decode(void* out, int32_t out_dtype, const void* query, const void* k_cac
     const int dev = current_device();
     if (dev < 0) return PA_ERR_CUDA;
     int* err = error_word(dev);
-    const int sms = sm_count(dev);
-    if (!err || sms <= 0) return PA_ERR_CUDA;
+    if (!err) return PA_ERR_CUDA;
 
-    int part = partition_size;
-    if (part == 0) {
-        // Enough independent (sequence, KV head, partition) items to keep
-        // every SM busy through the tail; shorter partitions when the batch
-        // is small.
-        const int64_t units = (int64_t)num_seqs * num_kv_heads;
-        part = units * max_parts_for(max_context_len, kAutoPartition) < 4LL * sms ? kAutoPartitionSmall
-                                                                                  : kAutoPartition;
-    }
+    const int part = pa::decode_partition(num_seqs, num_kv_heads, max_context_len, partition_size);
+    if (part <= 0) return PA_ERR_CUDA;
     const int max_parts = max_parts_for(max_context_len, part);
     const pa::DecodeWorkspaceLayout lay = pa::decode_workspace_layout(num_seqs, num_heads, max_parts, shape.head_dim);
     if (!aligned(workspace, 256) || workspace_bytes < lay.total) return PA_ERR_WORKSPACE;
@@ -302,18 +417,32 @@ int pa_decode(void* out, int32_t out_dtype, const void* query, const void* k_cac
     p.part_o = reinterpret_cast<float*>(ws + lay.part_o);
     p.err = err;
     p.wait_limit_ns = wait_limit_ns();
-    const char* drop = std::getenv("PA_DEBUG_DROP_FIRST_FILL");
-    p.debug_flags = (drop && drop[0] == '1') ? pa::kDebugDropFirstFill : 0;
+    p.debug_flags = option(PA_OPT_DROP_FIRST_FILL) ? pa::kDebugDropFirstFill : 0;
     // Every context fits one partition: no planning kernel, items are implicit.
     p.direct_items = max_parts == 1 ? (int)items_ub : 0;
 
-    pa::DecodeVariant variant = requested_variant();
-    CUtensorMap tmap_k, tmap_v;
-    if (cache->dtype == PA_F32 || !encode_pool_map(&tmap_k, k_cache, cache->dtype, shape) ||
-        !encode_pool_map(&tmap_v, v_cache, cache->dtype, shape))
-        variant = pa::kDecodeSimt;
+    if (option(PA_OPT_DEBUG_CHECKS)) {
+        rc = status_of(pa::launch_check_decode_inputs(context_lens, block_tables, num_seqs, max_blocks_per_seq,
+                                                      shape.block_size, max_context_len, shape.num_blocks, err,
+                                                      static_cast<cudaStream_t>(stream)));
+        if (rc != PA_OK) return rc;
+    }
+
+    pa::DecodeVariant variant = option(PA_OPT_DECODE_KERNEL) ? pa::kDecodeSimt : pa::kDecodeMma;
+    const CUtensorMap* tmap_k = nullptr;
+    const CUtensorMap* tmap_v = nullptr;
+    CUtensorMap k_map, v_map;  // copies: a second lookup may reuse the first one's cache slot
+    if (cache->dtype != PA_F32 && variant == pa::kDecodeMma) {
+        tmap_k = pool_map(k_cache, cache->dtype, shape, true);
+        if (tmap_k) {
+            k_map = *tmap_k;
+            tmap_v = pool_map(v_cache, cache->dtype, shape, true);
+        }
+        if (tmap_v) v_map = *tmap_v;
+    }
+    if (!tmap_k || !tmap_v) variant = pa::kDecodeSimt;
     return status_of(pa::launch_decode(p, cache->dtype, shape.head_dim, shape.block_size, group, (int)items_ub,
-                                       variant, &tmap_k, &tmap_v, static_cast<cudaStream_t>(stream)));
+                                       variant, &k_map, &v_map, static_cast<cudaStream_t>(stream)));
 }
 
 int pa_prefill(void* out, int32_t out_dtype, const void* query, const int32_t* query_start_loc,
@@ -321,6 +450,7 @@ int pa_prefill(void* out, int32_t out_dtype, const void* query, const int32_t* q
                const pa_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
                const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, float scale,
                void* stream) {
+    NvtxRange range("pa_prefill");
     pa::PoolShape shape;
     int rc = check_cache(cache, &shape);
     if (rc != PA_OK) return rc;
@@ -367,17 +497,21 @@ int pa_prefill(void* out, int32_t out_dtype, const void* query, const int32_t* q
     p.err = err;
     p.wait_limit_ns = wait_limit_ns();
 
-    CUtensorMap tmap_q, tmap_k, tmap_v;
-    if (!encode_query_map(&tmap_q, query, cache->dtype, num_query_tokens, num_heads, shape.head_dim, group) ||
-        !encode_pool_map(&tmap_k, k_cache, cache->dtype, shape, false) ||
-        !encode_pool_map(&tmap_v, v_cache, cache->dtype, shape, false))
-        return PA_ERR_UNSUPPORTED;
+    CUtensorMap tmap_q, tmap_k, tmap_v;  // copies: later lookups may reuse a cache slot
+    const CUtensorMap* m = query_map(query, cache->dtype, num_query_tokens, num_heads, shape.head_dim, group);
+    if (!m) return PA_ERR_UNSUPPORTED;
+    tmap_q = *m;
+    if (!(m = pool_map(k_cache, cache->dtype, shape, false))) return PA_ERR_UNSUPPORTED;
+    tmap_k = *m;
+    if (!(m = pool_map(v_cache, cache->dtype, shape, false))) return PA_ERR_UNSUPPORTED;
+    tmap_v = *m;
     return status_of(pa::launch_prefill(p, cache->dtype, shape.head_dim, &tmap_q, &tmap_k, &tmap_v,
                                         static_cast<cudaStream_t>(stream)));
 }
 
 int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers, const int64_t* src_dst_pairs,
                    int64_t num_pairs, const pa_cache_desc* cache, void* stream) {
+    NvtxRange range("pa_copy_blocks");
     pa::PoolShape shape;
     int rc = check_cache(cache, &shape);
     if (rc != PA_OK) return rc;
@@ -391,6 +525,10 @@ int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_lay
     if (dev < 0) return PA_ERR_CUDA;
     int* err = error_word(dev);
     if (!err) return PA_ERR_CUDA;
+    if (option(PA_OPT_DEBUG_CHECKS)) {
+        rc = status_of(pa::launch_check_pairs(src_dst_pairs, num_pairs, true, err, static_cast<cudaStream_t>(stream)));
+        if (rc != PA_OK) return rc;
+    }
     return status_of(pa::launch_copy_blocks(k_caches, v_caches, num_layers, src_dst_pairs, num_pairs, shape, err,
                                             static_cast<cudaStream_t>(stream)));
 }
@@ -411,6 +549,7 @@ bool gpu_addressable(const void* p) {
 int pa_swap_blocks(void* const* src_k, void* const* src_v, int64_t src_num_blocks, void* const* dst_k,
                    void* const* dst_v, int64_t dst_num_blocks, int32_t num_layers, const int64_t* src_dst_pairs,
                    int64_t num_pairs, const pa_cache_desc* cache, void* stream) {
+    NvtxRange range("pa_swap_blocks");
     pa::PoolShape shape;
     int rc = check_cache(cache, &shape);
     if (rc != PA_OK) return rc;
@@ -431,11 +570,20 @@ int pa_swap_blocks(void* const* src_k, void* const* src_v, int64_t src_num_block
             return PA_ERR_INVALID_ARG;
     int* err = error_word(dev);
     if (!err) return PA_ERR_CUDA;
+    if (option(PA_OPT_DEBUG_CHECKS)) {
+        bool same_pool = true;
+        for (int l = 0; l < num_layers; ++l)
+            if (src_k[l] != dst_k[l] || src_v[l] != dst_v[l]) same_pool = false;
+        rc = status_of(pa::launch_check_pairs(src_dst_pairs, num_pairs, same_pool, err,
+                                              static_cast<cudaStream_t>(stream)));
+        if (rc != PA_OK) return rc;
+    }
     return status_of(pa::launch_swap_blocks(src_k, src_v, src_num_blocks, dst_k, dst_v, dst_num_blocks, num_layers,
                                             src_dst_pairs, num_pairs, shape, err, static_cast<cudaStream_t>(stream)));
 }
 
 int pa_get_device_error(void* stream, int32_t* code) {
+    NvtxRange range("pa_get_device_error");
     if (!code) return PA_ERR_INVALID_ARG;
     *code = 0;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;

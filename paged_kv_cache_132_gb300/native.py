@@ -18,6 +18,8 @@ STATUS_NAMES = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED", 
                 -4: "PA_ERR_CUDA", -5: "PA_ERR_DEVICE_FAULT", -6: "PA_ERR_DEVICE_TIMEOUT"}
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_CONTEXT_LEN, DEVERR_COPY_PAIR, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
+DEVERR_DUP_SLOT, DEVERR_PAIR_CONFLICT = 0x20, 0x40  # checked mode only
+OPT_DEBUG_CHECKS, OPT_DECODE_KERNEL, OPT_DROP_FIRST_FILL = 0, 1, 2  # pa_option
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # PA_NOALLOC_SCRATCH_BYTES
 
 
@@ -70,8 +72,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.pa_status_string.argtypes = [ctypes.c_int]
         lib.pa_status_string.restype = ctypes.c_char_p
         lib.pa_abi_version.argtypes = []
+        lib.pa_set_option.argtypes = [ctypes.c_int, ctypes.c_int]
+        lib.pa_get_option.argtypes = [ctypes.c_int]
         for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_noalloc", "pa_copy_blocks",
-                     "pa_swap_blocks", "pa_prefill", "pa_get_device_error", "pa_abi_version"):
+                     "pa_swap_blocks", "pa_prefill", "pa_get_device_error", "pa_abi_version", "pa_set_option",
+                     "pa_get_option"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib

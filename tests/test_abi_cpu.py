@@ -1,6 +1,9 @@
 """The C-ABI library without a GPU: it loads, exports every declared symbol,
 and rejects bad arguments on the host before any CUDA call (CPU only)."""
 import ctypes
+import os
+import subprocess
+import sys
 
 import pytest
 
@@ -22,7 +25,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.pa_abi_version() == 1
+    assert lib.pa_abi_version() == 2
     for code, name in native.STATUS_NAMES.items():
         assert lib.pa_status_string(code).decode() == name
     assert lib.pa_status_string(-99).decode() == "PA_ERR_UNKNOWN"
@@ -162,3 +165,62 @@ def test_prefill_nothing_to_do_is_noop(lib):
     assert _prefill(lib, num_seqs=0) == 0
     assert _prefill(lib, tokens=0) == 0
     assert _prefill(lib, max_q=0) == 0
+
+
+def test_options_set_get_and_restore(lib):
+    for opt in (native.OPT_DEBUG_CHECKS, native.OPT_DECODE_KERNEL, native.OPT_DROP_FIRST_FILL):
+        before = lib.pa_get_option(opt)
+        assert before in (0, 1)
+        assert lib.pa_set_option(opt, 1) == before
+        assert lib.pa_get_option(opt) == 1
+        assert lib.pa_set_option(opt, 0) == 1
+        assert lib.pa_get_option(opt) == 0
+        lib.pa_set_option(opt, before)
+    assert lib.pa_set_option(3, 1) == -1      # unknown option
+    assert lib.pa_set_option(-1, 0) == -1
+    assert lib.pa_set_option(0, 2) == -1      # options are 0 or 1
+    assert lib.pa_get_option(7) == -1
+
+
+def test_option_api_context_manager(lib):
+    from paged_kv_cache_132_gb300 import api
+
+    assert not api.get_option("debug_checks")
+    with api.option("debug_checks"):
+        assert api.get_option("debug_checks")
+        with api.option("debug_checks", False):
+            assert not api.get_option("debug_checks")
+        assert api.get_option("debug_checks")
+    assert not api.get_option("debug_checks")
+
+
+_ENV_SCRIPT = """
+import sys
+sys.path.insert(0, {root!r})
+from paged_kv_cache_132_gb300 import native
+lib = native.load()
+print(lib.pa_get_option(native.OPT_DEBUG_CHECKS), lib.pa_get_option(native.OPT_DECODE_KERNEL),
+      lib.pa_get_option(native.OPT_DROP_FIRST_FILL))
+lib.pa_set_option(native.OPT_DEBUG_CHECKS, 0)
+print(lib.pa_get_option(native.OPT_DEBUG_CHECKS))
+"""
+
+
+@pytest.mark.parametrize("env,expect", [
+    ({"PA_DEBUG_CHECKS": "1", "PA_DECODE_KERNEL": "simt", "PA_DEBUG_DROP_FIRST_FILL": "1"}, "1 1 1"),
+    ({"PA_DEBUG_CHECKS": "0", "PA_DECODE_KERNEL": "mma"}, "0 0 0"),
+    ({}, "0 0 0"),
+])
+def test_options_start_from_the_environment(lib, env, expect):
+    """Each option's first value comes from its environment variable, read
+    once; pa_set_option overrides it afterwards."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    full = {k: v for k, v in os.environ.items()
+            if k not in ("PA_DEBUG_CHECKS", "PA_DECODE_KERNEL", "PA_DEBUG_DROP_FIRST_FILL")}
+    full.update(env)
+    r = subprocess.run([sys.executable, "-c", _ENV_SCRIPT.format(root=root)], env=full, capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    lines = r.stdout.split("\n")
+    assert lines[0].strip() == expect
+    assert lines[1].strip() == "0"

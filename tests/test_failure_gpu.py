@@ -1,7 +1,7 @@
 """Failure detection on the GPU without a fault: a bounded wait that runs out.
 
 Every wait inside the decode kernels is bounded by wall time
-(PA_WAIT_TIMEOUT_MS).  The test hook PA_DEBUG_DROP_FIRST_FILL=1 makes every
+(PA_WAIT_TIMEOUT_MS).  The test hook PA_OPT_DROP_FIRST_FILL makes every
 decode CTA leave its first pipeline stage unfilled -- a phase that nothing
 completes -- so the consumers' wait runs out.  The kernel must then record
 PA_DEVERR_TIMEOUT, drain its copies and return; the host reads
@@ -26,8 +26,7 @@ SCRIPT = textwrap.dedent("""
     from paged_kv_cache_132_gb300 import api, native, workloads
     native.load()
     for kernel in ("mma", "simt"):
-        if kernel == "simt":
-            os.environ["PA_DECODE_KERNEL"] = "simt"
+        api.set_option("decode_kernel_simt", kernel == "simt")
         w = workloads.make("llama8b", device="cuda", num_seqs=16)
         k, v = w.k_cache.clone(), w.v_cache.clone()
         api.reshape_and_cache(w.new_key, w.new_value, k, v, w.slot_mapping)
@@ -35,12 +34,12 @@ SCRIPT = textwrap.dedent("""
         run = lambda: api.decode(w.query, k, v, w.block_tables, w.context_lens, w.scale, max_context_len=mc)
         ref = run()
         assert api.get_device_error() == (0, 0)
-        os.environ["PA_DEBUG_DROP_FIRST_FILL"] = "1"
+        api.set_option("drop_first_fill", True)
         t0 = time.time()
         run()
         status, code = api.get_device_error()
         elapsed = time.time() - t0
-        del os.environ["PA_DEBUG_DROP_FIRST_FILL"]
+        api.set_option("drop_first_fill", False)
         assert status == -6 and code & 0x10, (status, code)
         assert elapsed < 20.0, elapsed
         again = run()

@@ -23,14 +23,11 @@ def _library():
 
 
 @pytest.fixture(params=["mma", "simt"])
-def kernel(request, monkeypatch):
+def kernel(request):
     """Run the test with the tensor-core decode kernel (the default for 16-bit
     pools) and again with the CUDA-core one."""
-    if request.param == "simt":
-        monkeypatch.setenv("PA_DECODE_KERNEL", "simt")
-    else:
-        monkeypatch.delenv("PA_DECODE_KERNEL", raising=False)
-    return request.param
+    with api.option("decode_kernel_simt", request.param == "simt"):
+        yield request.param
 
 
 def _check_step(w, **kw):
