@@ -47,7 +47,7 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from paged_kv_cache_132_gb300 import api, metrics, native, workloads  # noqa: E402
+from paged_kv_cache_132_gb300 import api, metrics, native, sharding, workloads  # noqa: E402
 
 WORKLOAD = "llama8b"
 METRIC = "paged decode-attention KV GB/s (% of GB300 HBM peak); seq-decode-steps/s"
@@ -59,7 +59,7 @@ PREFILL_KERNEL_SOURCES = ["prefill.cuh", "prefill_launch.cuh", "prefill_bf16.cu"
                           "common.cuh"]
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -81,7 +81,10 @@ def parse_args():
     ap.add_argument("--no-rows", action="store_true", help="skip the copy-on-write row timing")
     ap.add_argument("--decode-kernel", choices=["default", "simt"], default="default",
                     help="simt: time the CUDA-core decode kernel instead of the tensor-core one")
-    return ap.parse_args()
+    ap.add_argument("--split", choices=["replicas", "heads"], default="replicas",
+                    help="N > 1: replicas = each rank runs its own batch (weak scaling); heads = the ranks "
+                         "split one batch by KV head, same block tables on every rank (strong scaling)")
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -121,6 +124,28 @@ def measured_peaks():
             return json.load(f), "measured"
     except OSError:
         return {"hbm_gbs": 6800.0}, "fallback"
+
+
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo", encoding="utf-8") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.machine() or "unknown"
 
 
 class ClockSampler:
@@ -245,7 +270,21 @@ def cpu_baseline(w, target_seconds):
     return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{passes} full pass(es) of the {w.num_seqs}-sequence batch, fp64, "
                       f"OpenMP over (sequence, KV head), {total_t:.1f} s",
-            "single_thread_gbs": one_b / one_t / 1e9, "nproc": os.cpu_count()}
+            "single_thread_gbs": one_b / one_t / 1e9, "nproc": os.cpu_count(), "cpu_model": host_cpu_model()}
+
+
+def prefill_config(st, world):
+    """The `config` object of a prefill line, the same for both arms."""
+    dt = {torch.float16: "f16", torch.bfloat16: "bf16"}[st.dtype]
+    n_pairs = int(st.copy_pairs.shape[0])
+    return {"workload": f"{st.name}: {st.num_seqs} requests, prefixes {sorted(set(st.prefix_lens))}, "
+                        f"{st.num_tokens} new tokens (max chunk {st.max_query_len}), {st.num_heads} query / "
+                        f"{st.num_kv_heads} KV heads, d {st.head_dim}, {dt}, block {st.block_size}, "
+                        f"{n_pairs} copy-on-write pairs",
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (queries + outputs + pool above 129 MB); no flush",
+            "useful_flops_per_step": metrics.prefill_flops(st.attended_pairs(), st.num_heads, st.head_dim),
+            "attended_pairs_per_head": st.attended_pairs()}
 
 
 def run_reference_prefill(args):
@@ -265,17 +304,38 @@ def run_reference_prefill(args):
         tot_t += dt
         tot_f += last["value"] * 1e12 * dt
     value = tot_f / tot_t / 1e12
-    dt_name = {torch.float16: "f16", torch.bfloat16: "bf16"}[st.dtype]
     print(json.dumps({"impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s",
                       "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                       "ms_per_step": 1e3 * tot_t / max(args.steps, 1), "higher_is_better": True, "scaling": "weak",
                       "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                      "config": {"workload": f"{st.name}: {st.num_seqs} requests, {st.num_heads} query / "
-                                             f"{st.num_kv_heads} KV heads, d {st.head_dim}, {dt_name} inputs"},
+                      "config": prefill_config(st, max(args.gpus, 1)),
                       "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
-                                       "sample": last["sample"]},
+                                       "sample": last["sample"], "nproc": last["nproc"],
+                                       "cpu_model": last["cpu_model"]},
                       "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                               "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def decode_config(args, w, world, part, n_pairs, full_heads=None):
+    """The `config` object of a decode line, the same for both arms.
+    full_heads: (H, Hkv) of the whole batch when the ranks split it by head."""
+    ctx_list = w.context_lens.tolist()
+    elem = w.query.element_size()
+    dt = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}[w.dtype]
+    h, hkv = full_heads or (w.num_heads, w.num_kv_heads)
+    bytes_step = (metrics.decode_bytes(ctx_list, w.num_heads, w.num_kv_heads, w.head_dim, elem, 4)
+                  + metrics.write_bytes(w.num_tokens, w.num_kv_heads, w.head_dim, elem)
+                  + metrics.copy_bytes(n_pairs, 1, w.num_kv_heads, w.block_size, w.head_dim, elem))
+    if args.split == "heads":
+        parallelism = f"tp{world}: the batch split by KV head ({hkv // world} KV heads per rank, same block tables)"
+    else:
+        parallelism = f"replicas x{world}"
+    return {"workload": f"{args.workload}: {w.num_seqs} seqs, {h} query / {hkv} KV heads, d {w.head_dim}, "
+                        f"{dt} K/V, block {w.block_size}, partition {part}, {n_pairs} copy-on-write pairs",
+            "parallelism": parallelism,
+            "l2": "inputs larger than L2 (KV bytes per step far above the 129 MB L2); no flush",
+            "algorithmic_bytes_per_step": bytes_step, "sum_context_tokens": int(sum(ctx_list)),
+            "table_and_length_bytes_per_step": metrics.table_bytes(ctx_list, w.block_size)}
 
 
 def run_reference(args, rank, world):
@@ -313,10 +373,10 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / max(args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"{args.workload}: {w.num_seqs} seqs, {w.num_heads} query / {w.num_kv_heads} KV "
-                                   f"heads, d {w.head_dim}, block {w.block_size}"},
+            "config": decode_config(args, w, max(args.gpus, 1), partition_for(args, w), int(w.copy_pairs.shape[0])),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{n} random sequences of the batch per step"},
+                             "sample": f"{n} random sequences of the batch per step",
+                             "nproc": os.cpu_count(), "cpu_model": host_cpu_model()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -324,12 +384,21 @@ def run_reference(args, rank, world):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def make_workload(args, rank):
+def make_workload(args, rank, world=1):
+    """Rank `rank`'s batch: its own replica (seed per rank), or with
+    --split heads its KV heads of the one batch every rank draws alike."""
     kw = {"num_seqs": args.num_seqs}
     if args.workload == "long_context":
         kw["block_size"] = args.block_size
-    seed = workloads.SEED_BASE + workloads.WORKLOADS.index(args.workload) + 1000 * rank
-    return workloads.make(args.workload, device="cuda", seed=seed, **kw)
+    replica = 0 if args.split == "heads" else rank
+    seed = workloads.SEED_BASE + workloads.WORKLOADS.index(args.workload) + 1000 * replica
+    w = workloads.make(args.workload, device="cuda", seed=seed, **kw)
+    if args.split == "heads" and world > 1:
+        full = w
+        w = sharding.shard_workload(full, world, rank)
+        del full
+        torch.cuda.empty_cache()
+    return w
 
 
 def partition_for(args, w):
@@ -400,10 +469,41 @@ def swap_rows(w, stream, pairs_n=2048):
             "contiguous_d2h_memcpy_gbs": moved / (contiguous_us * 1e-6) / 1e9, "swap_pairs": n}
 
 
+def host_call_costs(w, out, ws, max_ctx, part, calls=40):
+    """Host time to submit one pa_decode call: through the Python binding
+    (argument checks, ctypes) and through ctypes with prepared arguments (the
+    C ABI's own cost: argument checks, cached tensor maps, the launches).  A
+    few calls at a time, so that the launch queue never fills."""
+    import ctypes
+
+    lib = native.load()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        api.decode(w.query, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, out=out,
+                   max_context_len=max_ctx, partition_size=part, workspace=ws)
+    py_us = 1e6 * (time.perf_counter() - t0) / calls
+    torch.cuda.synchronize()
+    desc = api.cache_desc(w.k_cache)
+    args_ = (out.data_ptr(), native.PA_F32, w.query.data_ptr(), w.k_cache.data_ptr(), w.v_cache.data_ptr(),
+             ctypes.byref(desc), w.block_tables.data_ptr(), w.block_tables.shape[1], w.context_lens.data_ptr(),
+             w.num_seqs, max_ctx, w.num_heads, w.num_kv_heads, ctypes.c_float(w.scale), part, ws.data_ptr(),
+             ws.numel(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        rc = lib.pa_decode(*args_)
+    c_us = 1e6 * (time.perf_counter() - t0) / calls
+    torch.cuda.synchronize()
+    if rc != 0:
+        raise RuntimeError(f"pa_decode returned {rc}")
+    return {"host_us_per_decode_call_python": py_us, "host_us_per_decode_call_c_abi": c_us}
+
+
 def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     native.load()
-    w = make_workload(args, rank)
+    w = make_workload(args, rank, world)
+    full_heads = (w.num_heads * world, w.num_kv_heads * world) if args.split == "heads" else None
     elem = w.query.element_size()
     ctx_list = w.context_lens.tolist()
     max_ctx = max(ctx_list)
@@ -478,6 +578,7 @@ def run_ours(args, rank, world, local_rank):
     write_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     decode_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
     step_ms = all_reduce_max(total_ms / k, world)
+    decode_ms_max = all_reduce_max(decode_ms, world)
     # Kernels per step: copy-on-write copy (if any pairs), cache write,
     # decode, and -- when a context can span more than one partition -- the
     # planning and cross-partition reduce kernels.
@@ -576,10 +677,18 @@ def run_ours(args, rank, world, local_rank):
         e2e_ms = all_reduce_max(s2.elapsed_time(e2) / k_e2e, world)
         launches_e2e = k_e2e * per_step
 
+    decode_call = lambda: api.decode(w.query, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
+                                     out=out, max_context_len=max_ctx, partition_size=part, workspace=ws)
     rows = {"a1_cache_write_us": 1e3 * write_ms, "a2_a6_decode_us": 1e3 * decode_ms,
             "a1_cache_write_median_us": 1e3 * statistics.median(e[1].elapsed_time(e[2]) for e in ev),
             "a2_a6_decode_median_us": 1e3 * statistics.median(e[2].elapsed_time(e[3]) for e in ev),
-            "step_graph_us": graph_time_us(step, 20, stream)}
+            "step_graph_us": graph_time_us(step, 20, stream),
+            # device time of back-to-back decode calls with no host gap (replayed from a CUDA graph)
+            "a2_a6_decode_warm_graph_us": graph_time_us(decode_call, 20, stream),
+            "a1_cache_write_graph_us": graph_time_us(
+                lambda: api.reshape_and_cache(w.new_key, w.new_value, w.k_cache, w.v_cache, w.slot_mapping), 20,
+                stream)}
+    rows.update(host_call_costs(w, out, ws, max_ctx, part))
     if not args.no_rows:
         # ---- cold decode calls: L2 flushed (a 2 x L2 buffer written) before each
         flush = torch.empty(2 * 129 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
@@ -623,12 +732,15 @@ def run_ours(args, rank, world, local_rank):
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
     achieved = decode_b / (decode_ms * 1e-3) / 1e9
-    traffic = profiled_traffic() if args.workload == WORKLOAD and args.num_seqs is None else None
+    traffic = (profiled_traffic() if args.workload == WORKLOAD and args.num_seqs is None and world == 1
+               else None)
     dt = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}[w.dtype]
-    desc = (f"{args.workload}: {w.num_seqs} seqs, {w.num_heads} query / {w.num_kv_heads} KV heads, d {w.head_dim}, "
-            f"{dt} K/V, block {w.block_size}, partition {part}, {n_pairs} copy-on-write pairs")
+    config = decode_config(args, w, world, part, n_pairs, full_heads)
+    assert config["algorithmic_bytes_per_step"] == bytes_step
     line = {
         "metric": METRIC,
+        # one step = the whole hot path (copy-on-write, cache write, decode);
+        # decode alone is "decode_gbs" below and the roofline object
         "value": aggregate_throughput(world, bytes_step, step_ms),
         "unit": "GB/s",
         "n_gpus": world,
@@ -636,15 +748,14 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup,
         "ms_per_step": step_ms,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong" if args.split == "heads" and world > 1 else "weak",
         "vs_baseline": None,
         "dtype": dt,
         "data": "synthetic",
-        "config": {"workload": desc, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (KV bytes per step far above the 129 MB L2); no flush",
-                   "algorithmic_bytes_per_step": bytes_step, "sum_context_tokens": int(sum(ctx_list)),
-                   "table_and_length_bytes_per_step": metrics.table_bytes(ctx_list, w.block_size)},
-        "seq_decode_steps_per_s": world * w.num_seqs / (step_ms * 1e-3),
+        "config": config,
+        "decode_gbs": aggregate_throughput(world, decode_b, decode_ms_max),
+        # with --split heads every rank decodes the same sequences (its heads)
+        "seq_decode_steps_per_s": (1 if args.split == "heads" else world) * w.num_seqs / (step_ms * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
                      "kernel": f"pa_decode ({'CUDA-core' if args.decode_kernel == 'simt' else 'tensor-core'} "
@@ -742,7 +853,7 @@ def prefill_cpu_baseline(st, target_seconds):
             break
     return {"value": flops / total_t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{done} whole sequence(s) of the step (shortest first), fp64, OpenMP over KV heads, "
-                      f"{total_t:.1f} s"}
+                      f"{total_t:.1f} s", "nproc": os.cpu_count(), "cpu_model": host_cpu_model()}
 
 
 def run_prefill(args, rank, world, local_rank):
@@ -847,13 +958,7 @@ def run_prefill(args, rank, world, local_rank):
         "unit": "TFLOP/s",
         "n_gpus": world, "steps": k_steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
-        "config": {"workload": f"{st.name}: {st.num_seqs} requests, prefixes {sorted(set(st.prefix_lens))}, "
-                               f"{st.num_tokens} new tokens (max chunk {st.max_query_len}), {st.num_heads} query / "
-                               f"{st.num_kv_heads} KV heads, d {st.head_dim}, {dt}, block {st.block_size}, "
-                               f"{n_pairs} copy-on-write pairs",
-                   "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (queries + outputs + pool above 129 MB); no flush",
-                   "useful_flops_per_step": flops, "attended_pairs_per_head": st.attended_pairs()},
+        "config": prefill_config(st, world),
         "new_tokens_per_s": world * st.num_tokens / (step_ms * 1e-3),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_kind} bf16_tflops (burst)",
@@ -953,7 +1058,7 @@ def run_beam(args, rank, world, local_rank):
 def main():
     args = parse_args()
     if args.decode_kernel == "simt":
-        os.environ["PA_DECODE_KERNEL"] = "simt"
+        api.set_option("decode_kernel_simt", True)
     rank, world, local_rank = dist_env()
     if world > 1:
         import torch.distributed as dist

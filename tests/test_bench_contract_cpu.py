@@ -6,6 +6,9 @@ import os
 import subprocess
 import sys
 
+import bench
+from paged_kv_cache_132_gb300 import workloads
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
@@ -30,3 +33,8 @@ def test_reference_arm_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    assert cpu["cpu_model"] and cpu["nproc"] >= 1
+    # the same config object as the repo's own arm prints for this workload
+    w = workloads.make("llama8b", device="cpu")
+    ours = bench.decode_config(bench.parse_args([]), w, 1, bench.partition_for(bench.parse_args([]), w), 0)
+    assert d["config"] == json.loads(json.dumps(ours))

@@ -45,6 +45,11 @@ def test_decode_line():
     d = run("--steps", "20", "--warmup", "3", "--cpu-seconds", "1", "--no-rows")
     check_common(d, "hbm", "GB/s")
     assert d["unit"] == "GB/s" and d["dtype"] == "bf16"
+    assert d["decode_gbs"] == pytest.approx(d["roofline"]["achieved"], rel=1e-6)
+    assert d["cpu_baseline"]["cpu_model"]
+    rows = d["rows"]
+    assert rows["host_us_per_decode_call_c_abi"] > 0 and rows["host_us_per_decode_call_python"] > 0
+    assert rows["a2_a6_decode_warm_graph_us"] > 0
 
 
 def test_prefill_line():
