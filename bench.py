@@ -805,6 +805,13 @@ def prefill_rows(stream, names=("prefill_llama8b", "prefill_opt13b")):
         status, code = api.get_device_error()
         if status != 0:
             raise RuntimeError(f"device error {status} ({code:#x}) in the {name} row")
+        write_us = graph_time_us(lambda: api.reshape_and_cache(st.new_key, st.new_value, k, v, st.slot_mapping),
+                                 10, stream)
+        write_b = metrics.write_bytes(st.num_tokens, st.num_kv_heads, st.head_dim, st.new_key.element_size())
+        hbm = float(peaks.get("hbm_gbs", 6800.0))
+        rows[f"{name}_cache_write_us"] = write_us
+        rows[f"{name}_cache_write_gbs"] = write_b / (write_us * 1e-6) / 1e9
+        rows[f"{name}_cache_write_frac_of_{kind}_hbm"] = write_b / (write_us * 1e-6) / 1e9 / hbm
         tflops = metrics.prefill_flops(st.attended_pairs(), st.num_heads, st.head_dim) / (call_us * 1e-6) / 1e12
         rows[f"{name}_call_us"] = call_us
         rows[f"{name}_tflops"] = tflops

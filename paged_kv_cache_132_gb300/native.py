@@ -48,6 +48,9 @@ def declared_symbols() -> list:
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
     """The loaded library; raises if it was not built."""
     global _lib
+    lib = _lib
+    if lib is not None and path == LIB_PATH:
+        return lib
     with _lock:
         if _lib is not None:
             return _lib
