@@ -140,6 +140,8 @@ struct PrefillParams {
     int ctx_cap;                  // max_blocks * block_size
     int tile_tokens;              // new tokens per CTA: 128 >> group_shift
     int tiles_per_seq;            // ceil(max_query_len / tile_tokens)
+    int tiles_adjacent;           // grid order: 1 = query tiles of a (sequence, KV head) adjacent
+                                  // (pools larger than L2), 0 = level by level
     float scale_log2;             // scale * log2(e)
     int* err;
     unsigned long long wait_limit_ns;

@@ -57,6 +57,15 @@ int* error_word(int dev) {
     return p;
 }
 
+int l2_bytes(int dev) {
+    static std::atomic<int> cached[kMaxDevices];
+    int n = cached[dev].load(std::memory_order_acquire);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) return 0;
+    cached[dev].store(n, std::memory_order_release);
+    return n;
+}
+
 int sm_count(int dev) {
     int n = g_sm_count[dev].load(std::memory_order_acquire);
     if (n > 0) return n;
@@ -493,6 +502,11 @@ int pa_prefill(void* out, int32_t out_dtype, const void* query, const int32_t* q
     p.ctx_cap = (int)(cap < 0x7fffffffLL ? cap : 0x7fffffffLL);
     p.tile_tokens = 128 / group;
     p.tiles_per_seq = (max_query_len + p.tile_tokens - 1) / p.tile_tokens;
+    // Pools (K and V) larger than L2: keep each (sequence, KV head)'s query
+    // tiles together so that its keys and values are read from HBM once.
+    const double pool_bytes = 2.0 * (double)shape.num_blocks * shape.num_kv_heads * shape.block_size *
+                              shape.head_dim * shape.elem_bytes;
+    p.tiles_adjacent = pool_bytes > (double)l2_bytes(dev) ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = err;
     p.wait_limit_ns = wait_limit_ns();

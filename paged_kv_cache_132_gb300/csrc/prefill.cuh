@@ -538,14 +538,26 @@ __global__ void __launch_bounds__(PrefillShape<D>::THREADS, PrefillShape<D>::CTA
     constexpr uint32_t IDESC_O = mma_idesc_f16(BF16, true, Shape::BM, D);
     extern __shared__ uint8_t prefill_smem_raw[];
 
-    // Block index -> (query tile, sequence, KV head); the last query tiles of
-    // every sequence (the longest key ranges) come first.
+    // Block index -> (query tile, sequence, KV head).  Level order (the
+    // default): the last query tiles of every sequence (the longest key
+    // ranges) first, then the next level, and so on.  When the pools exceed
+    // L2 every level would read them from HBM again, so then the query tiles
+    // of one (sequence, KV head) are adjacent instead (last tile first) and
+    // its keys and values stay in L2 while they are read.
     PrefillTile w;
     int u = blockIdx.x;
-    w.kv_head = u % p.num_kv_heads;
-    u /= p.num_kv_heads;
-    w.seq = u % p.num_seqs;
-    const int qt = p.tiles_per_seq - 1 - u / p.num_seqs;
+    int qt;
+    if (p.tiles_adjacent) {
+        qt = p.tiles_per_seq - 1 - u % p.tiles_per_seq;
+        u /= p.tiles_per_seq;
+        w.kv_head = u % p.num_kv_heads;
+        w.seq = u / p.num_kv_heads;
+    } else {
+        w.kv_head = u % p.num_kv_heads;
+        u /= p.num_kv_heads;
+        w.seq = u % p.num_seqs;
+        qt = p.tiles_per_seq - 1 - u / p.num_seqs;
+    }
 
     // The cache write before this kernel may still be finishing.
     pdl_wait_prerequisites();

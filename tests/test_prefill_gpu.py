@@ -180,6 +180,26 @@ def test_prefill_full_size_sampled(name):
     assert max_violation(got, ref) <= 0.0
 
 
+def test_prefill_grid_order_for_pools_larger_than_l2():
+    """Pools above the L2 size switch the grid to keep each (sequence, KV
+    head)'s query tiles together; every CTA computes the same tile either
+    way, so the outputs are bit-identical.  The same step is run on its own
+    pools and on the pools padded with unused (NaN) blocks past L2's size."""
+    st = workloads.make_prefill("prefill_tiny", device="cuda")
+    k, v, out, status, _ = gpu_prefill_step(st)
+    assert status == 0
+    block_bytes = k[0].numel() * k.element_size()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    pad = (l2 // block_bytes) // 2 + 1  # K and V together exceed L2
+    kp = torch.cat([k, torch.full((pad,) + tuple(k.shape[1:]), float("nan"), dtype=k.dtype, device="cuda")])
+    vp = torch.cat([v, torch.full((pad,) + tuple(v.shape[1:]), float("nan"), dtype=v.dtype, device="cuda")])
+    assert 2 * kp.numel() * kp.element_size() > l2
+    out2 = api.prefill(st.query, st.query_start_loc, kp, vp, st.block_tables, st.context_lens, st.scale,
+                       st.max_query_len)
+    assert api.get_device_error() == (0, 0)
+    assert torch.equal(out, out2)
+
+
 def test_prefill_relabelled_blocks_identical():
     """Moving every block to another physical id (and fixing the tables)
     leaves every output bit unchanged."""
