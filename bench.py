@@ -384,7 +384,7 @@ def run_reference(args, rank, world):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def make_workload(args, rank, world=1):
+def make_workload(args, rank, world=1, device="cuda"):
     """Rank `rank`'s batch: its own replica (seed per rank), or with
     --split heads its KV heads of the one batch every rank draws alike."""
     kw = {"num_seqs": args.num_seqs}
@@ -392,12 +392,13 @@ def make_workload(args, rank, world=1):
         kw["block_size"] = args.block_size
     replica = 0 if args.split == "heads" else rank
     seed = workloads.SEED_BASE + workloads.WORKLOADS.index(args.workload) + 1000 * replica
-    w = workloads.make(args.workload, device="cuda", seed=seed, **kw)
+    w = workloads.make(args.workload, device=device, seed=seed, **kw)
     if args.split == "heads" and world > 1:
         full = w
         w = sharding.shard_workload(full, world, rank)
         del full
-        torch.cuda.empty_cache()
+        if device == "cuda":
+            torch.cuda.empty_cache()
     return w
 
 
