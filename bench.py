@@ -472,9 +472,10 @@ def swap_rows(w, stream, pairs_n=2048):
 
 def host_call_costs(w, out, ws, max_ctx, part, calls=40):
     """Host time to submit one pa_decode call: through the Python binding
-    (argument checks, ctypes) and through ctypes with prepared arguments (the
-    C ABI's own cost: argument checks, cached tensor maps, the launches).  A
-    few calls at a time, so that the launch queue never fills."""
+    (argument checks, ctypes), through a prepared call (api.PreparedDecode:
+    checks done once) and through ctypes with prepared arguments (the C ABI's
+    own cost: argument checks, cached tensor maps, the launches).  A few calls
+    at a time, so that the launch queue never fills."""
     import ctypes
 
     lib = native.load()
@@ -484,6 +485,13 @@ def host_call_costs(w, out, ws, max_ctx, part, calls=40):
         api.decode(w.query, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, out=out,
                    max_context_len=max_ctx, partition_size=part, workspace=ws)
     py_us = 1e6 * (time.perf_counter() - t0) / calls
+    torch.cuda.synchronize()
+    prepared = api.PreparedDecode(w.query, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, out=out,
+                                  max_context_len=max_ctx, partition_size=part, workspace=ws)
+    t0 = time.perf_counter()
+    for _ in range(calls):
+        prepared()
+    prep_us = 1e6 * (time.perf_counter() - t0) / calls
     torch.cuda.synchronize()
     desc = api.cache_desc(w.k_cache)
     args_ = (out.data_ptr(), native.PA_F32, w.query.data_ptr(), w.k_cache.data_ptr(), w.v_cache.data_ptr(),
@@ -497,7 +505,8 @@ def host_call_costs(w, out, ws, max_ctx, part, calls=40):
     torch.cuda.synchronize()
     if rc != 0:
         raise RuntimeError(f"pa_decode returned {rc}")
-    return {"host_us_per_decode_call_python": py_us, "host_us_per_decode_call_c_abi": c_us}
+    return {"host_us_per_decode_call_python": py_us, "host_us_per_decode_call_prepared": prep_us,
+            "host_us_per_decode_call_c_abi": c_us}
 
 
 def run_ours(args, rank, world, local_rank):

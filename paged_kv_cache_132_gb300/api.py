@@ -117,6 +117,45 @@ def decode(query: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
     return out
 
 
+class PreparedDecode:
+    """A pa_decode call whose arguments are checked and marshalled once: for a
+    serving loop that decodes the same buffers every step (new contents, same
+    tensors), each call is then one C-ABI call with no per-call argument
+    checks.  The tensors are kept referenced; their shapes, dtypes, devices and
+    storage must not change while the object is used."""
+
+    def __init__(self, query: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, *, out: torch.Tensor,
+                 max_context_len: int, workspace: Optional[torch.Tensor] = None,
+                 num_kv_heads: Optional[int] = None, partition_size: int = 0):
+        self._lib = native.load()
+        _check_cuda(query, k_cache, v_cache, block_tables, context_lens, out)
+        _require(query.dim() == 3, "query is [num_seqs][num_heads][head_dim]")
+        s, h, d = query.shape
+        self._desc = cache_desc(k_cache)
+        _require(k_cache.shape == v_cache.shape and v_cache.dtype == k_cache.dtype, "K and V pools must match")
+        _require(query.dtype == k_cache.dtype and d == self._desc.head_dim, "query dtype/head_dim must match the pools")
+        _require(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == s,
+                 "block_tables is int32 [num_seqs][max_blocks]")
+        _require(context_lens.dtype == torch.int32 and context_lens.numel() == s, "context_lens is int32 [num_seqs]")
+        _require(out.shape == (s, h, d) and out.dtype in DTYPE_CODE, "out is [num_seqs][num_heads][head_dim]")
+        hkv = self._desc.num_kv_heads if num_kv_heads is None else num_kv_heads
+        if workspace is None:
+            need = decode_workspace_size(s, h, max_context_len, partition_size, d)
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=query.device)
+        _check_cuda(workspace)
+        self._keep = (query, k_cache, v_cache, block_tables, context_lens, out, workspace)
+        self.out = out
+        self._args = (out.data_ptr(), DTYPE_CODE[out.dtype], query.data_ptr(), k_cache.data_ptr(),
+                      v_cache.data_ptr(), ctypes.byref(self._desc), block_tables.data_ptr(), block_tables.shape[1],
+                      context_lens.data_ptr(), s, int(max_context_len), h, hkv, ctypes.c_float(float(scale)),
+                      int(partition_size), workspace.data_ptr(), workspace.numel())
+
+    def __call__(self, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+        _raise(self._lib.pa_decode(*self._args, _stream_ptr(stream)), "pa_decode")
+        return self.out
+
+
 def prefill(query: torch.Tensor, query_start_loc: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
             block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, max_query_len: int, *,
             num_kv_heads: Optional[int] = None, out: Optional[torch.Tensor] = None,

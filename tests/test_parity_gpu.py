@@ -246,6 +246,25 @@ def test_repeated_calls_reuse_workspace(kernel):
     assert torch.max(torch.abs(outs[0] - first)) < ATOL
 
 
+def test_prepared_decode_matches_decode(kernel):
+    """A decode call prepared once and run repeatedly (new contents of the same
+    tensors each time) gives what api.decode gives."""
+    w = workloads.make("llama8b", device="cuda", num_seqs=48)
+    k, v = w.k_cache.clone(), w.v_cache.clone()
+    api.reshape_and_cache(w.new_key, w.new_value, k, v, w.slot_mapping)
+    mc = int(w.context_lens.max())
+    q = w.query.clone()
+    out = torch.empty(w.num_seqs, w.num_heads, w.head_dim, device="cuda")
+    call = api.PreparedDecode(q, k, v, w.block_tables, w.context_lens, w.scale, out=out, max_context_len=mc,
+                              partition_size=512)
+    for step in range(3):
+        q.copy_(torch.roll(w.query, step, dims=0))  # new queries in the same buffer
+        got = call().clone()
+        ref = api.decode(q, k, v, w.block_tables, w.context_lens, w.scale, max_context_len=mc, partition_size=512)
+        assert api.get_device_error() == (0, 0)
+        assert torch.equal(got, ref)
+
+
 def test_step_captured_in_cuda_graph(kernel):
     """The step's calls can be captured in a CUDA graph (no allocation, no
     synchronisation inside them) and the replay gives the same outputs."""
