@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const __grid_
 }
 
 template <int D>
-__global__ void __launch_bounds__(kReduceThreads) decode_reduce_kernel(const __grid_constant__ DecodeParams p,
+__global__ void __launch_bounds__(kReduceThreads, 5) decode_reduce_kernel(const __grid_constant__ DecodeParams p,
                                                                         int group) {
     constexpr int VPL = D / 32;  // dims per lane (2 or 4)
     pdl_wait_prerequisites();    // the decode kernel wrote the partials
@@ -127,12 +127,38 @@ __global__ void __launch_bounds__(kReduceThreads) decode_reduce_kernel(const __g
 #pragma unroll
         for (int v = 0; v < VPL; ++v) acc[v] = 0.f;
         // Partitions in chunks of 32, lane q holding partition q's (m, l);
-        // a running max M and sum L carry the merge across chunks.
+        // a running max M and sum L carry the merge across chunks.  The
+        // outputs of a chunk's first kPre partitions are loaded together with
+        // the (m, l) pairs (they do not depend on them), so that most
+        // sequences (at most kPre partitions) wait for one round trip to L2,
+        // not two.
+        constexpr int kPre = 4;
         float M = NEG_INF, L = 0.f;
         for (int q0 = 0; q0 < nparts; q0 += 32) {
             float2 ml = make_float2(NEG_INF, 0.f);
             if (q0 + lane < nparts)
                 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + 2 * (base + (int64_t)(q0 + lane) * group)));
+            float pre[kPre][VPL];
+#pragma unroll
+            for (int k = 0; k < kPre; ++k) {
+                const float* src = p.part_o + (base + (int64_t)(q0 + k) * group) * D + lane * VPL;
+                if (q0 + k < nparts) {
+                    if constexpr (VPL == 4) {
+                        const float4 o = __ldcg(reinterpret_cast<const float4*>(src));
+                        pre[k][0] = o.x;
+                        pre[k][1] = o.y;
+                        pre[k][2] = o.z;
+                        pre[k][3] = o.w;
+                    } else {
+                        const float2 o = __ldcg(reinterpret_cast<const float2*>(src));
+                        pre[k][0] = o.x;
+                        pre[k][1] = o.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int v = 0; v < VPL; ++v) pre[k][v] = 0.f;
+                }
+            }
             float cm = ml.x;
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
@@ -147,8 +173,14 @@ __global__ void __launch_bounds__(kReduceThreads) decode_reduce_kernel(const __g
 #pragma unroll
             for (int v = 0; v < VPL; ++v) acc[v] *= rescale;
             const int n = min(32, nparts - q0);
-#pragma unroll 16
-            for (int k = 0; k < n; ++k) {
+#pragma unroll
+            for (int k = 0; k < kPre; ++k) {
+                const float wk = __shfl_sync(0xffffffffu, wq, k);  // 0 for k >= n
+#pragma unroll
+                for (int v = 0; v < VPL; ++v) acc[v] = fmaf(wk, pre[k][v], acc[v]);
+            }
+#pragma unroll 8
+            for (int k = kPre; k < n; ++k) {
                 const float wk = __shfl_sync(0xffffffffu, wq, k);
                 const float* src = p.part_o + (base + (int64_t)(q0 + k) * group) * D + lane * VPL;
                 if constexpr (VPL == 4) {
