@@ -166,3 +166,40 @@ def test_checked_step_matches_unchecked():
                                    max_context_len=w.max_context_len, partition_size=512))
             assert api.get_device_error() == (0, 0)
     assert torch.equal(outs[0], outs[1])
+
+
+def _pair_conflict(pairs, same_pool=True):
+    """Whether a pair list breaks the copy preconditions (plain Python)."""
+    dsts = [d for _, d in pairs]
+    if len(set(dsts)) != len(dsts):
+        return True
+    return same_pool and bool(set(dsts) & {s for s, _ in pairs})
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_lists_flag_exactly_the_violations(checked, seed):
+    """Random slot and pair lists, about half of them valid: the checked mode
+    sets its bit exactly when the list breaks a precondition."""
+    g = torch.Generator().manual_seed(seed)
+    w, k, v = _tiny()
+    nslots = w.num_blocks * w.block_size
+    n = int(torch.randint(1, 300, (1,), generator=g))
+    slots = torch.randperm(nslots * 8, generator=g)[:n] % nslots if seed % 2 else torch.randperm(nslots, generator=g)[:min(n, nslots)]
+    slots = slots.to(torch.int64)
+    slots[torch.rand(slots.numel(), generator=g) < 0.1] = -1  # padding tokens never conflict
+    valid = slots[slots >= 0]
+    expect = bool(valid.unique().numel() != valid.numel())
+    keys = torch.randn(slots.numel(), 4, 64, generator=g).cuda()
+    api.reshape_and_cache(keys, keys, k, v, slots.cuda())
+    status, code = api.get_device_error()
+    assert (code == native.DEVERR_DUP_SLOT) == expect and (status == -5) == expect, (seed, expect, code)
+    m = int(torch.randint(1, 40, (1,), generator=g))
+    pairs = torch.randint(0, w.num_blocks, (m, 2), generator=g)
+    if seed % 3 == 0:  # a valid list: distinct destinations, disjoint from the sources
+        blocks = torch.randperm(w.num_blocks, generator=g)
+        m = min(m, w.num_blocks // 2)
+        pairs = torch.stack([blocks[:m], blocks[m:2 * m]], dim=1)
+    expect = _pair_conflict(pairs.tolist())
+    api.copy_blocks([k], [v], pairs.cuda())
+    status, code = api.get_device_error()
+    assert (code == native.DEVERR_PAIR_CONFLICT) == expect and (status == -5) == expect, (seed, expect, code)

@@ -340,3 +340,16 @@ def test_beam_search_trace(kernel):
         ref = orc.decode(bits(st.query), kb, vb, O.BF16, st.block_tables.cpu().numpy(),
                          st.context_lens.cpu().numpy(), t.num_kv_heads, t.scale)
         assert max_violation(out, ref) <= 0.0
+
+
+@pytest.mark.parametrize("partition,max_len", [(64, 700), (0, 700), (512, 512)])
+def test_many_sequences(partition, max_len, kernel):
+    """3000 sequences: the planning kernel scans them in three chunks of 1024,
+    the reduce kernel strides over more (sequence, head) pairs than its grid
+    has warps, and -- with every context inside one partition -- the items map
+    to CTAs directly, many per CTA."""
+    g = torch.Generator().manual_seed(3000 + partition)
+    lens = torch.randint(1, max_len + 1, (3000,), generator=g).tolist()
+    w = workloads.custom(lens, num_heads=8, num_kv_heads=2, head_dim=64, block_size=16, dtype=torch.bfloat16,
+                         device="cuda", seed=3100 + partition)
+    _check_step(w, partition_size=partition)
