@@ -343,11 +343,11 @@ def test_beam_search_trace(kernel):
 
 
 @pytest.mark.parametrize("partition,max_len", [(64, 700), (0, 700), (512, 512)])
-def test_many_sequences(partition, max_len, kernel):
-    """3000 sequences: the planning kernel scans them in three chunks of 1024,
-    the reduce kernel strides over more (sequence, head) pairs than its grid
-    has warps, and -- with every context inside one partition -- the items map
-    to CTAs directly, many per CTA."""
+def test_many_sequences_each_kernel(partition, max_len, kernel):
+    """3000 sequences with both decode kernels: at partition 64 the reduce
+    kernel strides over more (sequence, head) pairs than its grid has warps,
+    and with every context inside one partition the items map to CTAs
+    directly, many per CTA."""
     g = torch.Generator().manual_seed(3000 + partition)
     lens = torch.randint(1, max_len + 1, (3000,), generator=g).tolist()
     w = workloads.custom(lens, num_heads=8, num_kv_heads=2, head_dim=64, block_size=16, dtype=torch.bfloat16,
