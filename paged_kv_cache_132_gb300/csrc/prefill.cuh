@@ -38,7 +38,8 @@
 //             table, one 2-D tensor copy per (block, 64-element slab), into
 //             a ring of slots released as soon as S_j has completed;
 //   warp 5    producer of the V tiles, likewise (slots released when
-//             P_j V_j has completed);
+//             P_j V_j has completed); it also zeroes the rows of the last V
+//             tile past kv_end (slots after the context may hold NaN);
 //   warp 6    MMA issuer (one thread) and owner of the TMEM allocation.
 // The MMA thread issues S_{j+1} before P_j.V_j, so the tensor cores compute
 // the next scores while the softmax warps work on the current ones.
@@ -91,6 +92,7 @@ struct PrefillShape {
         uint64_t s_full[2];    // S_j in buffer j % 2 (MMA commit)
         uint64_t p_full[2];    // P_j written over it (softmax warps)
         uint64_t pv_done[2];   // P_j V_j complete: buffer j % 2 free again
+        uint64_t v_tail;       // last V tile landed, its rows past kv_end zeroed (V producer)
         uint64_t mma_done;
         uint32_t tmem_base;
         int abort_flag;
@@ -218,6 +220,29 @@ __device__ void prefill_producer(const PrefillParams& p, typename Shape::Smem& s
         }
         if (!ok_run || *reinterpret_cast<volatile int*>(&sm.abort_flag)) break;
     }
+    if (!IS_K && ok_run) {
+        // The last V tile: rows past kv_end (slots after the context, blocks
+        // not loaded) may hold anything, NaN included; their weight is 0 but
+        // 0 * NaN is NaN, so they are zeroed before the last P.V reads the
+        // tile.  Done here rather than by the softmax warps, so that the
+        // tile's load latency does not delay the last P.
+        const int jl = w.nt - 1, st = jl % Shape::NSTAGE;
+        const int vrow0 = w.kv_end - jl * Shape::BN;
+        // Every lane observes the tile's arrival before writing into it.
+        const bool landed = mbar_wait_bounded(&full[st], (uint32_t)(jl / Shape::NSTAGE) & 1u, lim);
+        if (__all_sync(kFullMask, landed)) {
+            for (int idx = lane; idx < (Shape::BN - vrow0) * Shape::SLABS * 8; idx += 32) {
+                const int row = vrow0 + idx / (Shape::SLABS * 8);
+                const int rest = idx % (Shape::SLABS * 8);
+                reinterpret_cast<uint4*>(sm.v[st][rest >> 3] + row * 128)[rest & 7] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.v_tail);
+        } else {
+            ok_run = false;
+        }
+    }
     if (!ok_run && lane == 0) prefill_abort(p, sm);
     if (IS_K) pdl_launch_dependents();
     // Every copy this warp issued lands before the CTA exits (bounded).
@@ -296,7 +321,8 @@ __device__ void prefill_mma(const PrefillParams& p, typename Shape::Smem& sm, ui
             did = true;
         }
         if (jp < js && mbar_test(&sm.p_full[jp & 1], (uint32_t)(jp >> 1) & 1u) &&
-            mbar_test(&sm.v_full[jp % Shape::NSTAGE], (uint32_t)(jp / Shape::NSTAGE) & 1u)) {
+            (jp == nt - 1 ? mbar_test(&sm.v_tail, 0u)
+                          : mbar_test(&sm.v_full[jp % Shape::NSTAGE], (uint32_t)(jp / Shape::NSTAGE) & 1u))) {
             tc_fence_after_sync();
             issue_pv(jp++);
             did = true;
@@ -460,27 +486,6 @@ __device__ void prefill_softmax(const PrefillParams& p, typename Shape::Smem& sm
             }
         }
 
-        // Value rows past kv_end (slots after the context, blocks not loaded)
-        // may hold anything, NaN included; their weight is 0 but 0 * NaN is
-        // NaN, so the last tile's rows there are zeroed: row r & 63, half of
-        // its 16-byte chunks (by r / 64) in swizzled order.
-        const int vrow0 = w.kv_end - kv0;
-        if (j == w.nt - 1 && vrow0 < BN) {
-            const int st = j % Shape::NSTAGE;
-            ok = __all_sync(kFullMask,
-                            mbar_wait_bounded(&sm.v_full[st], (uint32_t)(j / Shape::NSTAGE) & 1u, lim));
-            if (!ok) break;
-            const int vr = r & (BN - 1), vh = r / BN;
-            if (vr >= vrow0) {
-#pragma unroll
-                for (int slab = 0; slab < Shape::SLABS; ++slab) {
-                    uint4* row = reinterpret_cast<uint4*>(sm.v[st][slab] + vr * 128);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) row[(vh * 4 + k) ^ (vr & 7)] = make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-            fence_proxy_async_smem();
-        }
         // A grown max rescales O, once P_{j-1} V_{j-1} has completed.
         if (j >= 1 && __any_sync(kFullMask, grow)) {
             const int pb = (j - 1) & 1;
@@ -590,6 +595,7 @@ __global__ void __launch_bounds__(PrefillShape<D>::THREADS, PrefillShape<D>::CTA
             mbar_init(&sm.p_full[b], Shape::SOFTMAX_WARPS);
             mbar_init(&sm.pv_done[b], 1);
         }
+        mbar_init(&sm.v_tail, 1);
         mbar_init(&sm.mma_done, 1);
         sm.abort_flag = 0;
         fence_mbar_init();
