@@ -520,11 +520,26 @@ __device__ void prefill_softmax(const PrefillParams& p, typename Shape::Smem& sm
         uint32_t u[32];
         tmem_ld_x32(row_addr + Shape::O_COL + c0, u);
         if (valid) {
+            if (p.out_dtype == PA_F32) {
 #pragma unroll
-            for (int k = 0; k < 32; k += 4)
-                store_out4(p.out, p.out_dtype, orow + c0 + k,
-                           make_float4(__uint_as_float(u[k]) * inv, __uint_as_float(u[k + 1]) * inv,
-                                       __uint_as_float(u[k + 2]) * inv, __uint_as_float(u[k + 3]) * inv));
+                for (int k = 0; k < 32; k += 4)
+                    store_out4(p.out, p.out_dtype, orow + c0 + k,
+                               make_float4(__uint_as_float(u[k]) * inv, __uint_as_float(u[k + 1]) * inv,
+                                           __uint_as_float(u[k + 2]) * inv, __uint_as_float(u[k + 3]) * inv));
+            } else {
+                // 16-bit output: eight values per 16-byte store
+#pragma unroll
+                for (int k = 0; k < 32; k += 8) {
+                    uint4 q;
+                    uint32_t* qw = reinterpret_cast<uint32_t*>(&q);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a = __uint_as_float(u[k + 2 * e]) * inv, b = __uint_as_float(u[k + 2 * e + 1]) * inv;
+                        qw[e] = p.out_dtype == PA_F16 ? pack_rn<__half>(a, b) : pack_rn<__nv_bfloat16>(a, b);
+                    }
+                    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow + c0 + k) = q;
+                }
+            }
         }
     }
 }
@@ -564,6 +579,12 @@ __global__ void __launch_bounds__(PrefillShape<D>::THREADS, PrefillShape<D>::CTA
         qt = p.tiles_per_seq - 1 - u / p.num_seqs;
     }
 
+    // Fetch the tensor-copy descriptors while the lengths load.
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tmap_q);
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+    }
     // The cache write before this kernel may still be finishing.
     pdl_wait_prerequisites();
     const int qs0 = __ldg(p.query_start + w.seq), qs1 = __ldg(p.query_start + w.seq + 1);
