@@ -160,6 +160,25 @@ def test_shared_prefix_equals_private_copies(kernel):
     assert torch.max(torch.abs(out - shared)) <= 1e-6
 
 
+def test_gqa_equals_repeated_mha(kernel):
+    """Invariant (5): a GQA step (8 KV heads, 32 query heads) gives what the
+    same step gives as MHA with every KV head repeated for its 4 query heads
+    (the pools and the new tokens repeated along the head axis)."""
+    w = workloads.make("llama8b", device="cuda", num_seqs=24)
+    g = w.num_heads // w.num_kv_heads
+    mha = dataclasses.replace(
+        w, num_kv_heads=w.num_heads,
+        k_cache=w.k_cache.repeat_interleave(g, dim=1).contiguous(),
+        v_cache=w.v_cache.repeat_interleave(g, dim=1).contiguous(),
+        new_key=w.new_key.repeat_interleave(g, dim=1).contiguous(),
+        new_value=w.new_value.repeat_interleave(g, dim=1).contiguous())
+    _, _, out_gqa, status, code = gpu_step(w, partition_size=512)
+    assert (status, code) == (0, 0)
+    _, _, out_mha, status, code = gpu_step(mha, partition_size=512)
+    assert (status, code) == (0, 0)
+    assert torch.max(torch.abs(out_gqa - out_mha)).item() <= 1e-6
+
+
 def test_copy_blocks_many_layers():
     layers, nb, hkv, bs, d = 3, 64, 4, 16, 128
     g = torch.Generator(device="cuda").manual_seed(11)
