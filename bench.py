@@ -53,7 +53,7 @@ WORKLOAD = "llama8b"
 METRIC = "paged decode-attention KV GB/s (% of GB300 HBM peak); seq-decode-steps/s"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_llama8b_ncu.md")
 PREFILL_METRIC = "paged prefill attention TFLOP/s (useful, causal pairs; % of GB300 bf16 tensor peak); new tokens/s"
-KERNEL_SOURCES = ["decode_mma.cuh", "decode_common.cuh", "decode.cu", "common.cuh"]
+KERNEL_SOURCES = ["decode_mma.cuh", "decode_common.cuh", "decode.cu", "common.cuh", "kernels.h"]
 PREFILL_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "prefill_llama8b_ncu.md")
 PREFILL_KERNEL_SOURCES = ["prefill.cuh", "prefill_launch.cuh", "prefill_bf16.cu", "tcgen05.cuh", "decode_common.cuh",
                           "common.cuh"]

@@ -9,7 +9,7 @@
 //    K come from the stage with ldmatrix.  The stage is filled by tensor
 //    copies with 128-byte swizzle (a line's 16-byte chunk k sits at k ^ (line
 //    % 8)), so the eight rows an ldmatrix reads fall in eight different bank
-//    groups (four with the interleaved layout of 8-token blocks).
+//    groups (four with the interleaved layout of 8- and 16-token blocks).
 //  * The accumulator of S has exactly the register layout of the A operand of
 //    P V (row g = lane/4, tokens 2j, 2j+1 and 8+2j, 8+2j+1 for j = lane%4),
 //    so the softmax runs in registers and P feeds the next MMA directly.

@@ -102,12 +102,17 @@ DecodeWorkspaceLayout decode_workspace_layout(int num_seqs, int num_heads, int m
 int decode_stage_tokens(int head_dim, int elem_bytes);
 
 // Stage layout of the tensor-core decode kernel.  A (block, head) tile of
-// head_dim 128 is two 128-byte column slabs per row.  With 8-token blocks a
-// tile is 2 KiB and is fetched as ONE box of a 3-D view [rows][2][64] --
-// rows interleaved in shared memory, 256 bytes apart -- because 1 KiB boxes
-// cost more per byte than the bandwidth allows; otherwise each slab is its
-// own box of the 2-D view [rows][d] and the stage keeps the slabs apart.
-constexpr bool interleaved_stage(int head_dim, int block_size) { return head_dim == 128 && block_size == 8; }
+// head_dim 128 is two 128-byte column slabs per row.  With 8- and 16-token
+// blocks a tile (2 or 4 KiB) is fetched as ONE box of a 3-D view
+// [rows][2][64] -- rows interleaved in shared memory, 256 bytes apart --
+// because each tensor copy has a cost of its own: 1 KiB boxes lose ~20% of
+// the bandwidth, and one 4 KiB box per tile instead of two 2 KiB slab boxes
+// is 0.5-2% faster.  With 32-token blocks (8 KiB tiles) each slab is its own
+// box of the 2-D view [rows][d] (measured no faster interleaved) and the
+// stage keeps the slabs apart.
+constexpr bool interleaved_stage(int head_dim, int block_size) {
+    return head_dim == 128 && (block_size == 8 || block_size == 16);
+}
 
 // Which decode consumer runs: the tensor-core one (16-bit pools, needs the
 // two tensor maps) or the CUDA-core one (every dtype).

@@ -160,7 +160,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // The pool [NB][Hkv][B][d] as a 2-D tensor of NB*Hkv*B rows of d 16-bit
 // elements; a box is 64 elements (128 bytes, the swizzle span) x B rows.
-// With interleave (the decode kernel, head_dim 128 and 8-token blocks) the
+// With interleave (the decode kernel, head_dim 128 and 8- or 16-token blocks) the
 // view is 3-D instead, one box per (block, head) tile.
 bool encode_pool_map(CUtensorMap* map, const void* base, int dtype, const pa::PoolShape& shape,
                      bool interleave = true) {
