@@ -190,10 +190,13 @@ __device__ inline void store_out4(void* out, int dtype, int64_t index, float4 v)
 // producer warp
 //   TENSOR = false: one linear bulk copy per (block, head) tile; the stage
 //                   holds rows in token order, ROW bytes apart.
-//   TENSOR = true : 2-D tensor copies with 128-byte swizzle, one box of
-//                   64 elements x BS rows per 128-byte column slab; the stage
-//                   holds slab s of row r at s*STAGE_TOK*128 + r*128, with
-//                   16-byte chunk c stored at chunk c ^ (r % 8).
+//   TENSOR = true : tensor copies with 128-byte swizzle.  Slab layout: one
+//                   2-D box of 64 elements x BS rows per 128-byte column slab;
+//                   the stage holds slab s of row r at s*STAGE_TOK*128 +
+//                   r*128, with 16-byte chunk c stored at chunk c ^ (r % 8).
+//                   Interleaved layout (Shape::INTERLEAVED): one 3-D box per
+//                   whole (block, head) tile; row r's two slabs at r*256 and
+//                   r*256 + 128, chunk c of line L = 2r + s at c ^ (L % 8).
 // ---------------------------------------------------------------------------
 template <class Shape, int BS, int G, bool TENSOR>
 __device__ void decode_producer(const DecodeParams& p, typename Shape::Smem& sm, int lane, const CUtensorMap* tk,
