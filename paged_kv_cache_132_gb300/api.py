@@ -71,6 +71,32 @@ def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Ten
                                     _stream_ptr(stream)), "pa_reshape_and_cache")
 
 
+class PreparedCacheWrite:
+    """A pa_reshape_and_cache call whose arguments are checked and marshalled
+    once: for a serving loop that writes each step's new tokens from the same
+    buffers (new contents, same tensors) into the same pools.  Each call is
+    then one C-ABI call.  The tensors are kept referenced; their shapes,
+    dtypes, devices and storage must not change while the object is used."""
+
+    def __init__(self, key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 slot_mapping: torch.Tensor):
+        self._lib = native.load()
+        _check_cuda(key, value, k_cache, v_cache, slot_mapping)
+        _require(k_cache.shape == v_cache.shape and k_cache.dtype == v_cache.dtype, "K and V pools must match")
+        _require(key.dtype == k_cache.dtype and value.dtype == k_cache.dtype, "key/value dtype must match the pools")
+        _require(key.dim() == 3 and key.shape == value.shape, "key/value are [num_tokens][num_kv_heads][head_dim]")
+        _require(tuple(key.shape[1:]) == (k_cache.shape[1], k_cache.shape[3]), "key/value heads or head_dim mismatch")
+        _require(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == key.shape[0],
+                 "slot_mapping is int64 [T]")
+        self._desc = cache_desc(k_cache)
+        self._keep = (key, value, k_cache, v_cache, slot_mapping)
+        self._args = (key.data_ptr(), value.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                      slot_mapping.data_ptr(), key.shape[0], ctypes.byref(self._desc))
+
+    def __call__(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+        _raise(self._lib.pa_reshape_and_cache(*self._args, _stream_ptr(stream)), "pa_reshape_and_cache")
+
+
 def decode_workspace_size(num_seqs: int, num_heads: int, max_context_len: int, partition_size: int = 0,
                           head_dim: int = 128) -> int:
     return int(native.load().pa_decode_workspace_size(num_seqs, num_heads, max_context_len, partition_size,

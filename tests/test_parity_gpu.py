@@ -284,6 +284,26 @@ def test_prepared_decode_matches_decode(kernel):
         assert torch.equal(got, ref)
 
 
+def test_prepared_cache_write_matches_reshape_and_cache():
+    """A cache write prepared once and run each step (new token contents and
+    slots in the same buffers) leaves the pools bit-identical to
+    api.reshape_and_cache."""
+    w = workloads.make("llama8b", device="cuda", num_seqs=48)
+    k1, v1 = w.k_cache.clone(), w.v_cache.clone()
+    k2, v2 = w.k_cache.clone(), w.v_cache.clone()
+    key, value, slots = w.new_key.clone(), w.new_value.clone(), w.slot_mapping.clone()
+    write = api.PreparedCacheWrite(key, value, k1, v1, slots)
+    for step in range(3):
+        key.copy_(torch.roll(w.new_key, step, dims=0))
+        value.copy_(torch.roll(w.new_value, step, dims=0))
+        slots.copy_(torch.roll(w.slot_mapping, step, dims=0))
+        write()
+        api.reshape_and_cache(key, value, k2, v2, slots)
+        assert api.get_device_error() == (0, 0)
+        assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+        assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
+
+
 def test_step_captured_in_cuda_graph(kernel):
     """The step's calls can be captured in a CUDA graph (no allocation, no
     synchronisation inside them) and the replay gives the same outputs."""
